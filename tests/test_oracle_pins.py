@@ -1,0 +1,284 @@
+"""Pins of the CPU oracle against things other than itself (no GPU).
+
+Each pin is chosen so that a plausible slip in the oracle fails it: a wrong sign
+in SiLU, sigmoid(-x) for sigmoid(x), a transposed operand, W1 and W2 swapped, a
+dropped term of the sum, rounding through float32 before bf16, or a wrong
+index in the packed layout.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import brute, compare, pack_layout
+from oracle.swiglu_ref import (bf16_bits_to_f64, f64_to_bf16_bits, gate_up_f64, silu,
+                               swiglu_f64, swiglu_f64_values)
+from swiglu_gated_mlp_gb300.workloads import bf16_bits, make_inputs
+
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "closed_forms.json")))
+
+
+def _frac(s):
+    from fractions import Fraction
+    return float(Fraction(s))
+
+
+def _example():
+    ex = GOLDEN["worked_example"]
+    a = np.array([[_frac(v) for v in r] for r in ex["A"]])
+    w1 = np.array([[_frac(v) for v in r] for r in ex["W1"]])
+    w2 = np.array([[_frac(v) for v in r] for r in ex["W2"]])
+    y = np.array([[float(v) for v in r] for r in ex["Y"]])
+    gate = np.array([[_frac(v) for v in r] for r in ex["gate_exact"]])
+    up = np.array([[_frac(v) for v in r] for r in ex["up_exact"]])
+    return a, w1, w2, gate, up, y
+
+
+# ---------------------------------------------------------------- SiLU ----
+
+@pytest.mark.parametrize("row", GOLDEN["silu"], ids=lambda r: r["x_name"])
+def test_silu_matches_symbolic_values(row):
+    x = float(row["x"])
+    want = float(row["silu"])
+    got = float(silu(np.float64(x)))
+    assert got == pytest.approx(want, rel=4e-16, abs=1e-300)
+
+
+@pytest.mark.parametrize("row", GOLDEN["silu_closed_forms"], ids=["ln3", "-ln3"])
+def test_silu_closed_forms(row):
+    assert float(silu(float(row["x"]))) == pytest.approx(float(row["silu"]), rel=4e-16)
+
+
+def test_silu_odd_part_is_identity():
+    # SiLU(x) - SiLU(-x) = x (sigmoid(x) + sigmoid(-x) = 1)
+    x = np.random.default_rng(0).normal(size=1000) * 8
+    assert np.allclose(silu(x) - silu(-x), x, rtol=1e-14, atol=1e-14)
+
+
+def test_silu_extremes_are_finite_and_signed():
+    assert silu(0.0) == 0.0
+    neg = silu(np.array([-1e4, -1e308, -800.0]))
+    assert np.all(neg == 0.0) and np.all(np.signbit(neg))
+    pos = silu(np.array([1e4, 800.0]))
+    assert np.array_equal(pos, [1e4, 800.0])
+    # -100 * e^-100 / (1 + e^-100), well inside float64 range
+    assert float(silu(-100.0)) == pytest.approx(-100.0 * math.exp(-100.0), rel=1e-15)
+
+
+# ------------------------------------------------------- worked example ----
+
+def test_worked_example_gate_up_exact():
+    a, w1, w2, gate, up, _ = _example()
+    g, u = gate_up_f64(a, w1, w2)
+    assert np.array_equal(g, gate) and np.array_equal(u, up)
+
+
+def test_worked_example_y():
+    a, w1, w2, _, _, y = _example()
+    assert np.allclose(swiglu_f64_values(a, w1, w2), y, rtol=1e-15, atol=0)
+
+
+def test_worked_example_through_bf16_bits():
+    a, w1, w2, _, _, y = _example()
+    got = swiglu_f64(f64_to_bf16_bits(a), f64_to_bf16_bits(w1), f64_to_bf16_bits(w2))
+    assert np.allclose(got, y, rtol=1e-15, atol=0)
+
+
+def test_brute_matches_worked_example():
+    a, w1, w2, _, _, y = _example()
+    got = np.array(brute.swiglu_brute(a.tolist(), w1.tolist(), w2.tolist()))
+    assert np.allclose(got, y, rtol=1e-15, atol=0)
+
+
+def test_swapping_w1_w2_changes_result():
+    a, w1, w2, _, _, y = _example()
+    assert not np.allclose(swiglu_f64_values(a, w2, w1), y, rtol=1e-3)
+
+
+def test_transposed_operand_is_caught():
+    # A (2x3) @ W (3x4): using W^T would need a 4x3 weight; a square case with a
+    # non-symmetric W shows the orientation instead.
+    a = np.array([[1.0, 2.0]])
+    w1 = np.array([[1.0, 0.0], [1.0, 1.0]])   # A @ W1 = [3, 2];  A @ W1^T = [1, 3]
+    w2 = np.eye(2)
+    y = swiglu_f64_values(a, w1, w2)
+    s = {r["x_name"]: float(r["silu"]) for r in GOLDEN["silu"]}
+    # Y = [SiLU(3) * 1, SiLU(2) * 2];  SiLU(3) = 3 sigmoid(3)
+    assert y[0, 1] == pytest.approx(s["2"] * 2, rel=1e-15)
+    assert y[0, 0] == pytest.approx(3.0 / (1.0 + math.exp(-3.0)), rel=1e-15)
+
+
+# ------------------------------------------------- brute force, tiny ----
+
+@pytest.mark.parametrize("shape", [(1, 1, 1), (3, 5, 7), (8, 16, 8), (9, 17, 33), (5, 64, 3)])
+def test_oracle_matches_brute_force(shape):
+    m, k, n = shape
+    a, w1, w2 = make_inputs(m, k, n, seed=m * 100 + k + n)
+    ab, w1b, w2b = bf16_bits(a), bf16_bits(w1), bf16_bits(w2)
+    av, w1v, w2v = (bf16_bits_to_f64(x) for x in (ab, w1b, w2b))
+    g_ref, u_ref = brute.gate_up_brute(av.tolist(), w1v.tolist(), w2v.tolist())
+    g, u = gate_up_f64(av, w1v, w2v)
+    # brute force is the exactly rounded sum; BLAS float64 is within K ulps
+    assert np.allclose(g, g_ref, rtol=k * 2.3e-16, atol=1e-300)
+    assert np.allclose(u, u_ref, rtol=k * 2.3e-16, atol=1e-300)
+    y_ref = np.array(brute.swiglu_brute(av.tolist(), w1v.tolist(), w2v.tolist()))
+    assert np.allclose(swiglu_f64(ab, w1b, w2b), y_ref, rtol=1e-13, atol=1e-15)
+
+
+def test_dropped_term_would_be_seen():
+    # every k contributes: zeroing one column of A changes Y on random data
+    a, w1, w2 = make_inputs(4, 32, 8, seed=11)
+    ab, w1b, w2b = bf16_bits(a), bf16_bits(w1), bf16_bits(w2)
+    y = swiglu_f64(ab, w1b, w2b)
+    for k in (0, 31):
+        ab2 = ab.copy()
+        ab2[:, k] = 0
+        assert not np.allclose(swiglu_f64(ab2, w1b, w2b), y, rtol=1e-6)
+
+
+# --------------------------------------------------------- identities ----
+
+def test_zero_activations_give_zero():
+    _, w1, w2 = make_inputs(1, 64, 40, seed=3)
+    a0 = np.zeros((7, 64), dtype=np.uint16)
+    y = swiglu_f64(a0, bf16_bits(w1), bf16_bits(w2))
+    assert np.array_equal(y, np.zeros((7, 40)))
+
+
+def test_linearity_in_w2():
+    a, w1, w2 = make_inputs(6, 48, 24, seed=5)
+    _, _, w2b = make_inputs(6, 48, 24, seed=6)
+    av, w1v, w2v, w2bv = (bf16_bits_to_f64(bf16_bits(x)) for x in (a, w1, w2, w2b))
+    y = swiglu_f64_values(av, w1v, w2v)
+    # scaling by 2 is exact in float64
+    assert np.array_equal(swiglu_f64_values(av, w1v, 2.0 * w2v), 2.0 * y)
+    y_sum = swiglu_f64_values(av, w1v, w2v + w2bv)
+    assert np.allclose(y_sum, y + swiglu_f64_values(av, w1v, w2bv), rtol=1e-12, atol=1e-13)
+
+
+def test_identity_slice_gives_silu_times_a():
+    # K = N, W1 = W2 = I:  Y = SiLU(A) (.) A; checked against the symbolic table
+    table = GOLDEN["silu"]
+    xs = np.array([float(r["x"]) for r in table])
+    want = np.array([float(r["silu"]) for r in table]) * xs
+    eye = np.eye(len(xs))
+    y = swiglu_f64_values(xs[None, :], eye, eye)[0]
+    assert np.allclose(y, want, rtol=1e-15, atol=1e-300)
+
+
+def test_one_hot_rows_select_weight_rows():
+    _, w1, w2 = make_inputs(1, 16, 12, seed=9)
+    w1v, w2v = bf16_bits_to_f64(bf16_bits(w1)), bf16_bits_to_f64(bf16_bits(w2))
+    a = np.zeros((3, 16))
+    picks = [0, 7, 15]
+    for m, k in enumerate(picks):
+        a[m, k] = 1.0
+    y = swiglu_f64_values(a, w1v, w2v)
+    want = np.array([[brute.silu_scalar(w1v[k, n]) * w2v[k, n] for n in range(12)] for k in picks])
+    assert np.allclose(y, want, rtol=1e-15, atol=0)
+
+
+def test_row_and_column_permutation_equivariance():
+    a, w1, w2 = make_inputs(10, 40, 20, seed=12)
+    ab, w1b, w2b = bf16_bits(a), bf16_bits(w1), bf16_bits(w2)
+    y = swiglu_f64(ab, w1b, w2b)
+    rp = np.random.default_rng(1).permutation(10)
+    cp = np.random.default_rng(2).permutation(20)
+    assert np.allclose(swiglu_f64(ab[rp], w1b, w2b), y[rp], rtol=1e-14, atol=1e-15)
+    assert np.allclose(swiglu_f64(ab, w1b[:, cp], w2b[:, cp]), y[:, cp], rtol=1e-14, atol=1e-15)
+
+
+def test_row_subset_equals_full_rows():
+    a, w1, w2 = make_inputs(33, 24, 16, seed=13)
+    ab, w1b, w2b = bf16_bits(a), bf16_bits(w1), bf16_bits(w2)
+    rows = np.array([0, 5, 32])
+    assert np.array_equal(swiglu_f64(ab, w1b, w2b, rows=rows), swiglu_f64(ab, w1b, w2b)[rows])
+
+
+# ------------------------------------------------------ bf16 rounding ----
+
+def test_bf16_bits_decode_known_patterns():
+    bits = np.array([0x3F80, 0xBF80, 0x0000, 0x8000, 0x7F80, 0x0001, 0x7F7F], dtype=np.uint16)
+    v = bf16_bits_to_f64(bits)
+    assert v[0] == 1.0 and v[1] == -1.0 and v[2] == 0.0 and np.signbit(v[3])
+    assert v[4] == np.inf and v[5] == 2.0 ** -133
+    assert v[6] == (2 - 2 ** -7) * 2.0 ** 127
+
+
+def test_bf16_rounding_ties_to_even_and_single_rounding():
+    one = 1.0
+    cases = {
+        one + 2 ** -8: 0x3F80,                 # halfway, round to even (down)
+        one + 3 * 2 ** -8: 0x3F82,             # halfway, round to even (up)
+        one + 2 ** -8 + 2 ** -30: 0x3F81,      # just above half: up; via float32 it would tie down
+        one + 2 ** -8 - 2 ** -30: 0x3F80,
+        -(one + 2 ** -8 + 2 ** -30): 0xBF81,
+        2.0 ** -130: 0x0008,                   # subnormal, exact
+        2.0 ** -134: 0x0000,                   # half the smallest subnormal: ties to even (0)
+        3 * 2.0 ** -134: 0x0002,               # 1.5 smallest subnormals: ties to even (2)
+        float.fromhex("0x1.ffp127"): 0x7F80,  # rounds past the largest finite: inf
+        float.fromhex("0x1.fe8p127") - 2.0 ** 100: 0x7F7F,  # just below the overflow threshold
+        -0.0: 0x8000,
+    }
+    xs = np.array(list(cases.keys()))
+    want = np.array(list(cases.values()), dtype=np.uint16)
+    assert np.array_equal(f64_to_bf16_bits(xs), want)
+    assert f64_to_bf16_bits(np.array([np.nan]))[0] == 0x7FC0
+
+
+def test_bf16_rounding_agrees_with_torch_on_float32_values():
+    # for values that are exactly float32, one rounding from float64 equals
+    # torch's float32 -> bf16 round-to-nearest-even
+    rng = np.random.default_rng(4)
+    x32 = np.concatenate([
+        rng.normal(size=20000).astype(np.float32) * np.float32(3),
+        (rng.normal(size=2000) * 1e-39).astype(np.float32),      # subnormals
+        rng.integers(0, 2 ** 32, size=20000, dtype=np.uint64).astype(np.uint32).view(np.float32),
+    ])
+    x32 = x32[np.isfinite(x32)]
+    want = torch.from_numpy(x32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = f64_to_bf16_bits(x32.astype(np.float64))
+    assert np.array_equal(got, want)
+
+
+# ------------------------------------------------------- comparison ----
+
+def test_ulp_distance_counts_bf16_steps():
+    ref = bf16_bits_to_f64(np.array([0x3F80, 0x3F80, 0x0000, 0x8001], dtype=np.uint16))
+    y = np.array([0x3F81, 0x3F7F, 0x8000, 0x0001], dtype=np.uint16)
+    assert compare.bf16_ulp_distance(y, ref).tolist() == [1, 1, 0, 2]
+
+
+def test_tolerance_rule_boundaries():
+    ref = np.array([1.0, 0.0, -2.0])
+    # bounds: 0.011 at ref=1, 0.001 at ref=0, 0.021 at ref=-2
+    y_ok = f64_to_bf16_bits(np.array([1.0078125, 0.0009765625, -2.015625]))
+    assert compare.within_tolerance(y_ok, ref).all()
+    y_bad = f64_to_bf16_bits(np.array([1.015625, 0.001953125, -2.0625]))
+    assert not compare.within_tolerance(y_bad, ref).any()
+    assert compare.mismatch_rate(y_bad, ref) == 1.0
+
+
+# ------------------------------------------------------ packed layout ----
+
+def test_pack_layout_indices_and_padding():
+    _, w1, w2 = make_inputs(1, 24, 200, seed=21)
+    w1b, w2b = bf16_bits(w1), bf16_bits(w2)
+    p = pack_layout.pack_reference(w1b, w2b)
+    assert p.shape == (2 * 256, 24)
+    blocks = p.reshape(2, 256, 24)
+    for n in (0, 1, 127, 128, 150, 199):
+        j, i = divmod(n, 128)
+        assert np.array_equal(blocks[j, i], w1b[:, n])
+        assert np.array_equal(blocks[j, 128 + i], w2b[:, n])
+    assert not blocks[1, 72:128].any() and not blocks[1, 128 + 72:].any()
+
+
+def test_pack_layout_round_trip():
+    _, w1, w2 = make_inputs(1, 40, 264, seed=22)
+    w1b, w2b = bf16_bits(w1), bf16_bits(w2)
+    u1, u2 = pack_layout.unpack_reference(pack_layout.pack_reference(w1b, w2b), 264)
+    assert np.array_equal(u1, w1b) and np.array_equal(u2, w2b)
