@@ -1,0 +1,176 @@
+/*
+ * swiglu.h - C ABI of libswiglu, the fused SwiGLU gated-MLP projection for
+ * NVIDIA GB300 (sm_103a).
+ *
+ *   Y = SiLU(A x W1) (.) (A x W2)
+ *
+ * Operation: "Tile-Level Activation Overlap for Efficient LLM Inference"
+ * (gist.science technical summary), section "Problem Statement": the gated MLP
+ * multiplies the activations by two weight matrices and gates one product with
+ * SiLU of the other. Section "Key Contributions" (tile-level fusion): the
+ * intermediate Gate = A x W1 and Up = A x W2 are never written to memory; here
+ * they live in fp32 tensor memory only.
+ *
+ * Types and layouts (all row-major, all bf16 unless stated):
+ *   A   [M, K]  activations, K contiguous.
+ *   W1  [K, N]  gate weight, N contiguous.   W2 [K, N] up weight, same layout.
+ *   Wp  packed gate/up weight produced by swiglu_pack_weights (opaque to
+ *       callers; layout stated at swiglu_pack_weights).
+ *   Y   [M, N]  output, N contiguous.
+ * Accumulation is fp32; SiLU(g) * u is evaluated in fp32 and rounded once to
+ * bf16 (round to nearest even).
+ *
+ * Ownership: every buffer is allocated, owned and freed by the caller; pointers
+ * are DEVICE pointers unless a parameter says "host". The library keeps one
+ * small device status word per device (allocated on first use) and never
+ * allocates on the forward path otherwise.
+ *
+ * Streams: every call is asynchronous on `stream` (a cudaStream_t; NULL means
+ * the legacy default stream). The return value reports argument errors and
+ * launch errors only; device-side faults of the kind the kernels can detect
+ * (a pipeline wait that ran past its time limit) are reported by
+ * swiglu_check_device_status.
+ *
+ * Thread safety: calls may be made from several host threads; one-time set-up
+ * per device is serialised internally.
+ */
+#ifndef SWIGLU_H_
+#define SWIGLU_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SWIGLU_API __attribute__((visibility("default")))
+#else
+#define SWIGLU_API
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* swiglu_stream_t;
+
+typedef enum {
+  SWIGLU_OK = 0,
+  SWIGLU_ERR_INVALID_ARG = 1, /* null/misaligned pointer, negative or zero size, aliasing */
+  SWIGLU_ERR_UNSUPPORTED = 2, /* K or N not a multiple of 8, size beyond limits, not sm_103 */
+  SWIGLU_ERR_CUDA = 3,        /* a CUDA runtime/driver call or a launch failed */
+  SWIGLU_ERR_TIMEOUT = 4,     /* a kernel's pipeline wait exceeded its limit (device-side) */
+  SWIGLU_ERR_NO_DEVICE = 5    /* no usable CUDA device / driver */
+} swiglu_status_t;
+
+/* Which kernel computes the forward pass. */
+typedef enum {
+  SWIGLU_VARIANT_AUTO = 0,    /* chosen from M (and the GPU's SM count) */
+  SWIGLU_VARIANT_LARGE_M = 1, /* 128-token tiles of A, weight columns as the MMA N side */
+  SWIGLU_VARIANT_SMALL_M = 2  /* weights as the MMA M side, tokens as N (M <= 256) */
+} swiglu_variant_t;
+
+/*
+ * Size in bytes of the packed weight for a K x N gate/up pair:
+ * 2 (matrices) * Np * K * 2 (bytes), Np = N rounded up to a multiple of 128.
+ * Returns 0 if K <= 0, N <= 0 or the size overflows.
+ */
+SWIGLU_API size_t swiglu_packed_weight_bytes(int64_t K, int64_t N);
+
+/*
+ * Pack W1 and W2 into the layout the forward kernels stream from.
+ *
+ * The pages fuse the two weights into one K x 2N matrix so that matching Gate
+ * and Up columns come out of one GEMM ("Tile-Level Activation Overlap for
+ * Efficient LLM Inference", gist.science, section "Methodology / Kernel-2":
+ * W_fused, even columns Gate, odd columns Up). This library interleaves blocks
+ * of 128 columns instead of single columns and stores each column
+ * K-contiguous:
+ *   Wp viewed as bf16 [Np/128][256][K]:
+ *     Wp[j][i][k]       = W1[k][j*128 + i]   (i < 128, gate)
+ *     Wp[j][128 + i][k] = W2[k][j*128 + i]   (i < 128, up)
+ *   and 0 for columns j*128 + i >= N.
+ *
+ * W1, W2: device, [K, N] bf16 row-major. Wpacked: device, at least
+ * swiglu_packed_weight_bytes(K, N) bytes, must not overlap W1 or W2.
+ * All three 16-byte aligned. Bit-exact copy; runs once per weight set.
+ * Errors: INVALID_ARG (null, misaligned, K<=0, N<=0, overlap), UNSUPPORTED
+ * (K or N not a multiple of 8, K or N above 2^21), NO_DEVICE, CUDA.
+ */
+SWIGLU_API swiglu_status_t swiglu_pack_weights(const void* W1, const void* W2, void* Wpacked,
+                                               int64_t K, int64_t N, swiglu_stream_t stream);
+
+/*
+ * Y = SiLU(A x W1) (.) (A x W2), fused ("Tile-Level Activation Overlap for
+ * Efficient LLM Inference", gist.science, sections "Problem Statement" and
+ * "Methodology"): one pass over the packed weight; Gate and Up accumulate in
+ * tensor memory, SiLU and the product run in the epilogue, Y is stored once.
+ *
+ * A: device [M, K] bf16. Wpacked: device, from swiglu_pack_weights with the
+ * same K and N. Y: device [M, N] bf16, written in full, must not overlap A or
+ * Wpacked. All 16-byte aligned.
+ * M = 0 is a no-op returning OK.
+ * Errors: INVALID_ARG (null or misaligned pointer, M < 0, K <= 0, N <= 0,
+ * overlap), UNSUPPORTED (K or N not a multiple of 8; M above 2^31-1; K or N
+ * above 2^21; device not sm_103), NO_DEVICE, CUDA (launch failure).
+ */
+SWIGLU_API swiglu_status_t swiglu_forward(const void* A, const void* Wpacked, void* Y,
+                                          int64_t M, int64_t K, int64_t N,
+                                          swiglu_stream_t stream);
+
+/*
+ * swiglu_forward with an explicit kernel choice (swiglu_variant_t); the
+ * result is the same within rounding. SMALL_M requires M <= 256 (else
+ * UNSUPPORTED).
+ */
+SWIGLU_API swiglu_status_t swiglu_forward_variant(const void* A, const void* Wpacked, void* Y,
+                                                  int64_t M, int64_t K, int64_t N,
+                                                  int variant, swiglu_stream_t stream);
+
+/*
+ * End-to-end form for callers whose activations live in host memory:
+ * copies A_host -> A_dev, runs swiglu_forward(A_dev, Wpacked, Y_dev), copies
+ * Y_dev -> Y_host, all enqueued on `stream` in that order (asynchronous: the
+ * caller synchronises before reading Y_host). A_host and Y_host are HOST
+ * pointers (page-locked memory gives asynchronous copies); A_dev and Y_dev are
+ * caller-owned device staging buffers of 2*M*K and 2*M*N bytes.
+ * Errors: as swiglu_forward, plus INVALID_ARG for null host pointers.
+ */
+SWIGLU_API swiglu_status_t swiglu_forward_from_host(const void* A_host, const void* Wpacked,
+                                                    void* Y_host, void* A_dev, void* Y_dev,
+                                                    int64_t M, int64_t K, int64_t N,
+                                                    swiglu_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word. Returns SWIGLU_ERR_TIMEOUT if any kernel since the last check gave up
+ * on a pipeline wait (every wait in the kernels is bounded; the kernel then
+ * stops cleanly and releases its resources), SWIGLU_ERR_CUDA if the stream
+ * reports an error, SWIGLU_OK otherwise.
+ */
+SWIGLU_API swiglu_status_t swiglu_check_device_status(swiglu_stream_t stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+SWIGLU_API const char* swiglu_status_string(swiglu_status_t status);
+
+/*
+ * Describes, as one line of text in `buf` (NUL-terminated, truncated to
+ * `buflen`), the kernel and tiling swiglu_forward_variant would use for this
+ * shape on the current device, e.g. "large_m bn=128 stages=4 tiles=4736
+ * grid=152". Returns a status like swiglu_forward's argument checks.
+ */
+SWIGLU_API swiglu_status_t swiglu_plan_string(int64_t M, int64_t K, int64_t N, int variant,
+                                              char* buf, size_t buflen);
+
+/*
+ * Testing hook for the failure path: while `enable` is non-zero, the next
+ * forward launches skip one pipeline-stage fill, so a wait inside the kernel
+ * runs out after `timeout_ms` milliseconds (default 1000) and the kernel exits
+ * with SWIGLU_ERR_TIMEOUT recorded. `timeout_ms` = 0 keeps the current limit.
+ */
+SWIGLU_API void swiglu_testing_inject_stall(int enable, uint32_t timeout_ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWIGLU_H_ */

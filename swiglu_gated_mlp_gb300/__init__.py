@@ -1,1 +1,24 @@
-"""Fused SwiGLU gated-MLP projection for GB300 (sm_103a): Y = SiLU(A W1) * (A W2)."""
+"""Fused SwiGLU gated-MLP projection for NVIDIA GB300 (sm_103a).
+
+    Y = SiLU(A W1) * (A W2),   A [M, K], W1 / W2 [K, N], Y [M, N], all bf16.
+
+The public functions mirror the C ABI in include/swiglu.h (same names):
+``swiglu_pack_weights``, ``swiglu_forward``, ``swiglu_forward_variant``,
+``swiglu_forward_from_host``, ``swiglu_packed_weight_bytes``,
+``swiglu_check_device_status``, ``swiglu_status_string``, ``swiglu_plan_string``.
+They load the compiled library on first use and raise if it is missing; there
+is no CPU or PyTorch fallback.
+"""
+_EXPORTS = {
+    "swiglu_pack_weights", "swiglu_forward", "swiglu_forward_variant", "swiglu_forward_from_host",
+    "swiglu_packed_weight_bytes", "swiglu_check_device_status", "swiglu_status_string",
+    "swiglu_plan_string", "swiglu_testing_inject_stall", "SwigluError",
+    "SWIGLU_VARIANT_AUTO", "SWIGLU_VARIANT_LARGE_M", "SWIGLU_VARIANT_SMALL_M",
+}
+
+
+def __getattr__(name):
+    if name in _EXPORTS:
+        from . import _native
+        return getattr(_native, name)
+    raise AttributeError(name)

@@ -1,0 +1,178 @@
+"""Thin ctypes binding of libswiglu (include/swiglu.h), with the same names.
+
+Argument marshalling only: every step of the computation runs in the library's
+CUDA kernels. PyTorch supplies device memory and the current stream. There is
+no fallback: if the library is not built, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB_PATH
+
+SWIGLU_OK = 0
+SWIGLU_ERR_INVALID_ARG = 1
+SWIGLU_ERR_UNSUPPORTED = 2
+SWIGLU_ERR_CUDA = 3
+SWIGLU_ERR_TIMEOUT = 4
+SWIGLU_ERR_NO_DEVICE = 5
+
+SWIGLU_VARIANT_AUTO = 0
+SWIGLU_VARIANT_LARGE_M = 1
+SWIGLU_VARIANT_SMALL_M = 2
+
+PACK_BLOCK_N = 128
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is not built; run `python -m swiglu_gated_mlp_gb300.build` "
+        "(or __graft_entry__.build()) first")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_i64, _vp, _sz, _int, _u32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_uint32
+lib.swiglu_packed_weight_bytes.argtypes = [_i64, _i64]
+lib.swiglu_packed_weight_bytes.restype = _sz
+lib.swiglu_pack_weights.argtypes = [_vp, _vp, _vp, _i64, _i64, _vp]
+lib.swiglu_pack_weights.restype = _int
+lib.swiglu_forward.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _vp]
+lib.swiglu_forward.restype = _int
+lib.swiglu_forward_variant.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]
+lib.swiglu_forward_variant.restype = _int
+lib.swiglu_forward_from_host.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]
+lib.swiglu_forward_from_host.restype = _int
+lib.swiglu_check_device_status.argtypes = [_vp]
+lib.swiglu_check_device_status.restype = _int
+lib.swiglu_status_string.argtypes = [_int]
+lib.swiglu_status_string.restype = ctypes.c_char_p
+lib.swiglu_plan_string.argtypes = [_i64, _i64, _i64, _int, ctypes.c_char_p, _sz]
+lib.swiglu_plan_string.restype = _int
+lib.swiglu_testing_inject_stall.argtypes = [_int, _u32]
+lib.swiglu_testing_inject_stall.restype = None
+
+
+class SwigluError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {swiglu_status_string(code)}")
+
+
+def _check(code: int, where: str) -> None:
+    if code != SWIGLU_OK:
+        raise SwigluError(code, where)
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream) if isinstance(stream, torch.cuda.Stream) else int(stream)
+
+
+def _dev_bf16(t: torch.Tensor, name: str) -> None:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != torch.bfloat16:
+        raise ValueError(f"{name} must be bfloat16, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def padded_n(n: int) -> int:
+    return -(-int(n) // PACK_BLOCK_N) * PACK_BLOCK_N
+
+
+def swiglu_status_string(code: int) -> str:
+    return lib.swiglu_status_string(int(code)).decode()
+
+
+def swiglu_packed_weight_bytes(K: int, N: int) -> int:
+    return int(lib.swiglu_packed_weight_bytes(int(K), int(N)))
+
+
+def swiglu_pack_weights(W1: torch.Tensor, W2: torch.Tensor, Wpacked: torch.Tensor | None = None,
+                        stream=None) -> torch.Tensor:
+    """Packed gate/up weight (bf16 [2*Np, K]) from W1, W2 [K, N] (bf16, CUDA)."""
+    _dev_bf16(W1, "W1")
+    _dev_bf16(W2, "W2")
+    if W1.dim() != 2 or W1.shape != W2.shape:
+        raise ValueError("W1 and W2 must both be [K, N]")
+    K, N = W1.shape
+    if Wpacked is None:
+        Wpacked = torch.empty((2 * padded_n(N), K), dtype=torch.bfloat16, device=W1.device)
+    _dev_bf16(Wpacked, "Wpacked")
+    if Wpacked.numel() * 2 < swiglu_packed_weight_bytes(K, N):
+        raise ValueError("Wpacked is too small")
+    with torch.cuda.device(W1.device):
+        _check(lib.swiglu_pack_weights(W1.data_ptr(), W2.data_ptr(), Wpacked.data_ptr(), K, N,
+                                       _stream_handle(stream, W1.device)), "swiglu_pack_weights")
+    return Wpacked
+
+
+def swiglu_forward_variant(A: torch.Tensor, Wpacked: torch.Tensor, N: int, variant: int,
+                           Y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    _dev_bf16(A, "A")
+    _dev_bf16(Wpacked, "Wpacked")
+    if A.dim() != 2:
+        raise ValueError("A must be [M, K]")
+    M, K = A.shape
+    if Wpacked.numel() * 2 < swiglu_packed_weight_bytes(K, N):
+        raise ValueError("Wpacked does not hold a packed weight for this K and N")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _dev_bf16(Y, "Y")
+    if tuple(Y.shape) != (M, N):
+        raise ValueError("Y must be [M, N]")
+    with torch.cuda.device(A.device):
+        _check(lib.swiglu_forward_variant(A.data_ptr(), Wpacked.data_ptr(), Y.data_ptr(), M, K, N,
+                                          int(variant), _stream_handle(stream, A.device)),
+               "swiglu_forward")
+    return Y
+
+
+def swiglu_forward(A: torch.Tensor, Wpacked: torch.Tensor, N: int, Y: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
+    """Y [M, N] = SiLU(A W1) * (A W2) from A [M, K] and the packed weight."""
+    return swiglu_forward_variant(A, Wpacked, N, SWIGLU_VARIANT_AUTO, Y=Y, stream=stream)
+
+
+def swiglu_forward_from_host(A_host: torch.Tensor, Wpacked: torch.Tensor, N: int,
+                             Y_host: torch.Tensor, A_dev: torch.Tensor, Y_dev: torch.Tensor,
+                             stream=None) -> torch.Tensor:
+    """Host A -> device, fused forward, device Y -> host, all enqueued on `stream`."""
+    for t, name in ((A_host, "A_host"), (Y_host, "Y_host")):
+        if t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bfloat16 host tensor")
+    _dev_bf16(Wpacked, "Wpacked")
+    _dev_bf16(A_dev, "A_dev")
+    _dev_bf16(Y_dev, "Y_dev")
+    M, K = A_host.shape
+    if tuple(A_dev.shape) != (M, K) or tuple(Y_host.shape) != (M, N) or tuple(Y_dev.shape) != (M, N):
+        raise ValueError("shape mismatch between host and device buffers")
+    with torch.cuda.device(A_dev.device):
+        _check(lib.swiglu_forward_from_host(A_host.data_ptr(), Wpacked.data_ptr(), Y_host.data_ptr(),
+                                            A_dev.data_ptr(), Y_dev.data_ptr(), M, K, N,
+                                            _stream_handle(stream, A_dev.device)),
+               "swiglu_forward_from_host")
+    return Y_host
+
+
+def swiglu_check_device_status(stream=None, device=None) -> None:
+    """Synchronises the stream; raises SwigluError if a kernel reported a timeout."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(device):
+        _check(lib.swiglu_check_device_status(_stream_handle(stream, device)),
+               "swiglu_check_device_status")
+
+
+def swiglu_plan_string(M: int, K: int, N: int, variant: int = SWIGLU_VARIANT_AUTO) -> str:
+    buf = ctypes.create_string_buffer(256)
+    _check(lib.swiglu_plan_string(int(M), int(K), int(N), int(variant), buf, 256),
+           "swiglu_plan_string")
+    return buf.value.decode()
+
+
+def swiglu_testing_inject_stall(enable: bool, timeout_ms: int = 0) -> None:
+    lib.swiglu_testing_inject_stall(1 if enable else 0, int(timeout_ms))

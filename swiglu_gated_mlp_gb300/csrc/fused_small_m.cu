@@ -1,0 +1,211 @@
+// Small-M (decode) fused SwiGLU kernel: Y = SiLU(A W1) * (A W2) for M <= 256.
+//
+// With few tokens the op is bound by streaming the weights from HBM once. The
+// pages give small batches to Kernel-2 because its doubled threadblock count
+// fills the SMs ("Tile-Level Activation Overlap for Efficient LLM Inference",
+// gist.science, section "Methodology / Kernel-2", Optimization). Here the
+// operands are swapped instead: each CTA owns one 128-column block of the
+// packed weight (128 gate rows + 128 up rows, K-contiguous) and streams it
+// through a deep TMA ring; the weight rows are the MMA's M side (128) and the
+// tokens its N side (mt = M rounded up to 16), so
+//   Gate^T[128 x mt] = W1_block^T * A^T   and   Up^T likewise,
+// two tcgen05.mma per K step into two fp32 TMEM accumulators. The epilogue
+// thread for weight column n reads gate and up for all tokens, applies
+// SiLU(g) * u in fp32 and writes Y[m][n] (a warp writes 32 consecutive
+// columns of one row at a time).
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace swg {
+namespace {
+
+constexpr int kWStageBytes = 2 * kPackBlockN * kBlockK * 2;  // 32 KB: 256 packed rows x 128 B
+constexpr int kMaxStages = 8;
+constexpr size_t kSmemLimit = 232448;
+constexpr int kBarBytes = 256;
+
+__global__ void __launch_bounds__(kThreads, 1)
+    fused_small_m_kernel(const __grid_constant__ SmallMParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int mt = p.mt;
+  const int stages = p.stages;
+  const uint32_t x_bytes = static_cast<uint32_t>(mt) * kBlockK * 2;
+  const uint32_t stage_bytes = kWStageBytes + x_bytes;  // multiple of 1024 (mt % 8 == 0)
+  const uint32_t s0 = smem_addr(smem);
+  uint8_t* bar_ptr = smem + size_t(stages) * stage_bytes;
+  const uint32_t bar0 = smem_addr(bar_ptr);
+  // barrier slots: full[8] | empty[8] | tmem_full | drain
+  const uint32_t full0 = bar0, empty0 = bar0 + 8u * kMaxStages;
+  const uint32_t tfull_bar = bar0 + 16u * kMaxStages, drain_bar = tfull_bar + 8u;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_ptr + 8 * (2 * kMaxStages + 2));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  uint32_t tmem_cols = 32;
+  while (tmem_cols < 2u * mt) tmem_cols <<= 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int num_kb = (p.K + kBlockK - 1) / kBlockK;
+  const int nblk = blockIdx.x;
+  const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
+
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&p.tmap_x);
+    prefetch_tmap(&p.tmap_w);
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(full0 + 8u * s, 1);
+      mbar_init(empty0 + 8u * s, 1);
+    }
+    mbar_init(tfull_bar, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer -----
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();  // weights: read once
+      const uint64_t pol_x = policy_evict_last();   // activations: re-read by every CTA
+      const int wrow = nblk * 2 * kPackBlockN;
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t filled = 0, fill_ph = 0;
+      bool skip_once = p.inject_stall != 0;
+      for (int kb = 0; kb < num_kb; ++kb) {
+        if (!mbar_wait(empty0 + 8u * s, ph ^ 1u, wc, kSiteProducerEmpty)) break;
+        if (skip_once) {
+          skip_once = false;  // testing hook: leave this stage unfilled
+        } else {
+          const uint32_t fb = full0 + 8u * s;
+          const uint32_t sw = s0 + s * stage_bytes;
+          const int k0 = kb * kBlockK;
+          mbar_arrive_expect_tx(fb, stage_bytes);
+          tma_load_2d_hint(sw, &p.tmap_w, fb, k0, wrow, pol_w);
+          tma_load_2d_hint(sw + kWStageBytes, &p.tmap_x, fb, k0, 0, pol_x);
+          filled |= 1u << s;
+          fill_ph = (fill_ph & ~(1u << s)) | (ph << s);
+        }
+        if (++s == stages) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      for (int i = 0; i < stages; ++i)
+        if (filled & (1u << i)) mbar_wait_drain(full0 + 8u * i, (fill_ph >> i) & 1u, wc);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer -------
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(128, mt);
+      const uint32_t d_gate = tmem_base;
+      const uint32_t d_up = tmem_base + static_cast<uint32_t>(mt);
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int kb = 0; kb < num_kb; ++kb) {
+        if (!mbar_wait(full0 + 8u * s, ph, wc, kSiteMmaFull)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sw = s0 + s * stage_bytes;
+        const uint64_t gdesc = smem_desc_sw128(sw);                         // gate rows 0..127
+        const uint64_t udesc = smem_desc_sw128(sw + kWStageBytes / 2);      // up rows 128..255
+        const uint64_t xdesc = smem_desc_sw128(sw + kWStageBytes);          // tokens
+#pragma unroll
+        for (int k = 0; k < kBlockK / 16; ++k) {
+          const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
+          mma_bf16(d_gate, gdesc + 2u * k, xdesc + 2u * k, idesc, acc);
+          mma_bf16(d_up, udesc + 2u * k, xdesc + 2u * k, idesc, acc);
+        }
+        mma_commit(empty0 + 8u * s);
+        if (++s == stages) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      if (ok) mma_commit(tfull_bar);
+      mma_commit(drain_bar);
+      mbar_wait_drain(drain_bar, 0, wc);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ epilogue ---------
+    const int q = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const int n = nblk * kPackBlockN + q * 32 + lane;  // this thread's output column
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(tfull_bar, 0, wc, kSiteEpiTmemFull) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) {
+      tc_fence_after();
+      __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(p.y);
+#pragma unroll 1
+      for (int mc = 0; mc < mt / 16; ++mc) {
+        uint32_t g[16], u[16];
+        tmem_ld_x16(tmem_base + lane_off + mc * 16, g);
+        tmem_ld_x16(tmem_base + lane_off + mt + mc * 16, u);
+        tmem_wait_ld();
+        reg_fence(g);
+        reg_fence(u);
+        if (n < p.N) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int m = mc * 16 + j;
+            if (m < p.M)
+              y[static_cast<size_t>(m) * p.N + n] =
+                  __float2bfloat16_rn(silu_mul(__uint_as_float(g[j]), __uint_as_float(u[j])));
+          }
+        }
+      }
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, tmem_cols);
+  }
+}
+
+}  // namespace
+
+int small_m_stages(int mt) {
+  const size_t stage = kWStageBytes + size_t(mt) * kBlockK * 2;
+  const size_t avail = kSmemLimit - 1024 - kBarBytes;
+  size_t s = avail / stage;
+  if (s > kMaxStages) s = kMaxStages;
+  return static_cast<int>(s);
+}
+
+size_t small_m_smem_bytes(int mt, int stages) {
+  return 1024 + size_t(stages) * (kWStageBytes + size_t(mt) * kBlockK * 2) + kBarBytes;
+}
+
+cudaError_t configure_small_m() {
+  return cudaFuncSetAttribute(fused_small_m_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(kSmemLimit));
+}
+
+cudaError_t launch_small_m(const SmallMParams& p, cudaStream_t stream) {
+  if (p.stages < 2 || p.stages > kMaxStages || p.mt < 16 || p.mt > 256 || (p.mt % 16) != 0)
+    return cudaErrorInvalidValue;
+  fused_small_m_kernel<<<p.grid, kThreads, small_m_smem_bytes(p.mt, p.stages), stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace swg

@@ -1,0 +1,58 @@
+// Host-side launch interface of the device kernels (internal to libswiglu).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace swg {
+
+constexpr int kPackBlockN = 128;  // columns per gate/up block of the packed weight
+constexpr int kBlockK = 64;       // K elements per pipeline stage (128 B rows, 128-B swizzle)
+constexpr int kTileM = 128;       // tokens per large-M tile (MMA M)
+constexpr int kThreads = 192;     // 6 warps: TMA producer, MMA issuer, 4 epilogue warps
+
+struct LargeMParams {
+  CUtensorMap tmap_a;  // A  [M, K]       box {64, 128}, 128-B swizzle
+  CUtensorMap tmap_w;  // Wp [2*Np, K]    box {64, bn},  128-B swizzle
+  CUtensorMap tmap_y;  // Y  [M, N]       box {32, 32},  64-B swizzle (store)
+  int M, K, N;
+  int tiles_m, tiles_n, group_m;
+  int bn;    // output columns per tile: 32, 64 or 128 (MMA N = 2 * bn)
+  int grid;  // persistent CTAs
+  uint32_t* status;
+  uint64_t timeout_ns;
+  int inject_stall;
+};
+
+struct SmallMParams {
+  CUtensorMap tmap_x;  // A  [M, K]     box {64, mt}, 128-B swizzle
+  CUtensorMap tmap_w;  // Wp [2*Np, K]  box {64, 256}, 128-B swizzle
+  void* y;             // Y  [M, N] bf16
+  int M, K, N;
+  int mt;      // tokens rounded up to a multiple of 16 (MMA N), <= 256
+  int stages;  // pipeline depth
+  int grid;    // one CTA per 128-column block
+  uint32_t* status;
+  uint64_t timeout_ns;
+  int inject_stall;
+};
+
+// One-time per-device set-up (dynamic shared-memory limits of every instantiation).
+cudaError_t configure_large_m();
+cudaError_t configure_small_m();
+
+int large_m_stages(int bn);
+size_t large_m_smem_bytes(int bn);
+cudaError_t launch_large_m(const LargeMParams& p, cudaStream_t stream);
+
+int small_m_stages(int mt);
+size_t small_m_smem_bytes(int mt, int stages);
+cudaError_t launch_small_m(const SmallMParams& p, cudaStream_t stream);
+
+cudaError_t launch_pack(const void* w1, const void* w2, void* wp, int K, int N,
+                        cudaStream_t stream);
+
+}  // namespace swg

@@ -1,0 +1,376 @@
+// libswiglu C ABI: argument checks, per-device set-up, TMA descriptor encoding,
+// kernel choice and launch. Declarations and contracts are in include/swiglu.h.
+#include "swiglu.h"
+
+#include <atomic>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "kernels.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxKN = int64_t(1) << 21;
+constexpr int64_t kMaxM = 2147483647;
+
+struct DeviceState {
+  std::atomic<bool> ready{false};
+  swiglu_status_t init_status = SWIGLU_OK;
+  int sm_count = 0;
+  uint32_t* status = nullptr;  // uint32_t[4], see ptx.cuh
+};
+
+DeviceState g_dev[kMaxDevices];
+std::mutex g_init_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::atomic<int> g_inject{0};
+std::atomic<uint64_t> g_timeout_ns{1000000000ull};
+
+int64_t env_int(const char* name, int64_t dflt) {
+  const char* v = std::getenv(name);
+  if (!v || !*v) return dflt;
+  char* end = nullptr;
+  const long long x = std::strtoll(v, &end, 10);
+  return (end && *end == '\0') ? static_cast<int64_t>(x) : dflt;
+}
+
+// Largest M for which AUTO picks the small-M (weights-as-MMA-M) kernel.
+int64_t small_m_max() {
+  static const int64_t v = env_int("SWIGLU_SMALL_M_MAX", 64);
+  return v;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + bn && b0 < a0 + an;
+}
+
+int64_t padded_n(int64_t n) {
+  return (n + swg::kPackBlockN - 1) / swg::kPackBlockN * swg::kPackBlockN;
+}
+
+swiglu_status_t init_device(int dev, DeviceState& d) {
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_ERR_NO_DEVICE;
+  }
+  if (major != 10 || minor != 3) return SWIGLU_ERR_UNSUPPORTED;  // built for sm_103a only
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+      cudaGetLastError();
+      return SWIGLU_ERR_CUDA;
+    }
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  if (cudaMalloc(&d.status, 4 * sizeof(uint32_t)) != cudaSuccess ||
+      cudaMemset(d.status, 0, 4 * sizeof(uint32_t)) != cudaSuccess ||
+      swg::configure_large_m() != cudaSuccess || swg::configure_small_m() != cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_ERR_CUDA;
+  }
+  return SWIGLU_OK;
+}
+
+swiglu_status_t device_state(DeviceState** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_ERR_NO_DEVICE;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return SWIGLU_ERR_UNSUPPORTED;
+  DeviceState& d = g_dev[dev];
+  if (!d.ready.load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(g_init_mu);
+    if (!d.ready.load(std::memory_order_relaxed)) {
+      d.init_status = init_device(dev, d);
+      d.ready.store(true, std::memory_order_release);
+    }
+  }
+  *out = &d;
+  return d.init_status;
+}
+
+bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swizzle) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Plan {
+  int variant = SWIGLU_VARIANT_AUTO;
+  int bn = 0, stages = 0, tiles_m = 0, tiles_n = 0, group_m = 0, tiles = 0, grid = 0, mt = 0;
+};
+
+swiglu_status_t make_plan(int64_t M, int64_t N, int variant, int sm_count, Plan* pl) {
+  if (variant != SWIGLU_VARIANT_AUTO && variant != SWIGLU_VARIANT_LARGE_M &&
+      variant != SWIGLU_VARIANT_SMALL_M)
+    return SWIGLU_ERR_INVALID_ARG;
+  if (variant == SWIGLU_VARIANT_AUTO)
+    variant = (M <= small_m_max() && M <= 256) ? SWIGLU_VARIANT_SMALL_M : SWIGLU_VARIANT_LARGE_M;
+  const int64_t np = padded_n(N);
+  pl->variant = variant;
+  if (variant == SWIGLU_VARIANT_SMALL_M) {
+    if (M > 256) return SWIGLU_ERR_UNSUPPORTED;
+    pl->mt = static_cast<int>((M + 15) / 16 * 16);
+    pl->stages = swg::small_m_stages(pl->mt);
+    pl->tiles = static_cast<int>(np / swg::kPackBlockN);
+    pl->grid = pl->tiles;
+    return SWIGLU_OK;
+  }
+  const int64_t tiles_m = (M + swg::kTileM - 1) / swg::kTileM;
+  int bn = 32;
+  for (int cand : {128, 64, 32}) {
+    if (tiles_m * (np / cand) >= sm_count) {
+      bn = cand;
+      break;
+    }
+  }
+  const int64_t tiles = tiles_m * (np / bn);
+  if (tiles > 2147483647) return SWIGLU_ERR_UNSUPPORTED;
+  pl->bn = bn;
+  pl->stages = swg::large_m_stages(bn);
+  pl->tiles_m = static_cast<int>(tiles_m);
+  pl->tiles_n = static_cast<int>(np / bn);
+  pl->group_m = static_cast<int>(tiles_m < 16 ? tiles_m : 16);
+  pl->tiles = static_cast<int>(tiles);
+  pl->grid = static_cast<int>(tiles < sm_count ? tiles : sm_count);
+  return SWIGLU_OK;
+}
+
+swiglu_status_t check_shape(int64_t M, int64_t K, int64_t N) {
+  if (M < 0 || K <= 0 || N <= 0) return SWIGLU_ERR_INVALID_ARG;
+  if ((K % 8) != 0 || (N % 8) != 0) return SWIGLU_ERR_UNSUPPORTED;  // 16-byte TMA row stride
+  if (M > kMaxM || K > kMaxKN || N > kMaxKN) return SWIGLU_ERR_UNSUPPORTED;
+  return SWIGLU_OK;
+}
+
+swiglu_status_t check_forward_args(const void* A, const void* Wp, const void* Y, int64_t M,
+                                   int64_t K, int64_t N) {
+  const swiglu_status_t st = check_shape(M, K, N);
+  if (st != SWIGLU_OK || M == 0) return st;
+  if (!A || !Wp || !Y) return SWIGLU_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(Wp) || !aligned16(Y)) return SWIGLU_ERR_INVALID_ARG;
+  const size_t a_bytes = size_t(M) * size_t(K) * 2, y_bytes = size_t(M) * size_t(N) * 2;
+  const size_t w_bytes = swiglu_packed_weight_bytes(K, N);
+  if (overlaps(Y, y_bytes, A, a_bytes) || overlaps(Y, y_bytes, Wp, w_bytes))
+    return SWIGLU_ERR_INVALID_ARG;
+  return SWIGLU_OK;
+}
+
+swiglu_status_t launch_forward(const void* A, const void* Wp, void* Y, int64_t M, int64_t K,
+                               int64_t N, const Plan& pl, DeviceState& d, cudaStream_t stream) {
+  const int64_t np = padded_n(N);
+  const uint64_t timeout = g_timeout_ns.load();
+  const int inject = g_inject.load();
+  cudaError_t err;
+  if (pl.variant == SWIGLU_VARIANT_SMALL_M) {
+    swg::SmallMParams p{};
+    if (!encode_2d(&p.tmap_x, A, K, M, K * 2, swg::kBlockK, pl.mt,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&p.tmap_w, Wp, K, 2 * np, K * 2, swg::kBlockK, 2 * swg::kPackBlockN,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+      return SWIGLU_ERR_CUDA;
+    p.y = Y;
+    p.M = static_cast<int>(M);
+    p.K = static_cast<int>(K);
+    p.N = static_cast<int>(N);
+    p.mt = pl.mt;
+    p.stages = pl.stages;
+    p.grid = pl.grid;
+    p.status = d.status;
+    p.timeout_ns = timeout;
+    p.inject_stall = inject;
+    err = swg::launch_small_m(p, stream);
+  } else {
+    swg::LargeMParams p{};
+    if (!encode_2d(&p.tmap_a, A, K, M, K * 2, swg::kBlockK, swg::kTileM,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&p.tmap_w, Wp, K, 2 * np, K * 2, swg::kBlockK, pl.bn,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&p.tmap_y, Y, N, M, N * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+      return SWIGLU_ERR_CUDA;
+    p.M = static_cast<int>(M);
+    p.K = static_cast<int>(K);
+    p.N = static_cast<int>(N);
+    p.tiles_m = pl.tiles_m;
+    p.tiles_n = pl.tiles_n;
+    p.group_m = pl.group_m;
+    p.bn = pl.bn;
+    p.grid = pl.grid;
+    p.status = d.status;
+    p.timeout_ns = timeout;
+    p.inject_stall = inject;
+    err = swg::launch_large_m(p, stream);
+  }
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_ERR_CUDA;
+  }
+  return SWIGLU_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t swiglu_packed_weight_bytes(int64_t K, int64_t N) {
+  if (K <= 0 || N <= 0 || K > kMaxKN || N > kMaxKN) return 0;
+  return size_t(2) * size_t(padded_n(N)) * size_t(K) * 2;
+}
+
+swiglu_status_t swiglu_pack_weights(const void* W1, const void* W2, void* Wpacked, int64_t K,
+                                    int64_t N, swiglu_stream_t stream) {
+  swiglu_status_t st = check_shape(0, K, N);
+  if (st != SWIGLU_OK) return st;
+  if (!W1 || !W2 || !Wpacked) return SWIGLU_ERR_INVALID_ARG;
+  if (!aligned16(W1) || !aligned16(W2) || !aligned16(Wpacked)) return SWIGLU_ERR_INVALID_ARG;
+  const size_t w_bytes = size_t(K) * size_t(N) * 2;
+  const size_t p_bytes = swiglu_packed_weight_bytes(K, N);
+  if (overlaps(Wpacked, p_bytes, W1, w_bytes) || overlaps(Wpacked, p_bytes, W2, w_bytes))
+    return SWIGLU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != SWIGLU_OK) return st;
+  if (swg::launch_pack(W1, W2, Wpacked, static_cast<int>(K), static_cast<int>(N),
+                       reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_ERR_CUDA;
+  }
+  return SWIGLU_OK;
+}
+
+swiglu_status_t swiglu_forward_variant(const void* A, const void* Wpacked, void* Y, int64_t M,
+                                       int64_t K, int64_t N, int variant,
+                                       swiglu_stream_t stream) {
+  swiglu_status_t st = check_forward_args(A, Wpacked, Y, M, K, N);
+  if (st != SWIGLU_OK) return st;
+  if (variant < SWIGLU_VARIANT_AUTO || variant > SWIGLU_VARIANT_SMALL_M)
+    return SWIGLU_ERR_INVALID_ARG;
+  if (M == 0) return SWIGLU_OK;
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != SWIGLU_OK) return st;
+  Plan pl;
+  st = make_plan(M, N, variant, d->sm_count, &pl);
+  if (st != SWIGLU_OK) return st;
+  return launch_forward(A, Wpacked, Y, M, K, N, pl, *d, reinterpret_cast<cudaStream_t>(stream));
+}
+
+swiglu_status_t swiglu_forward(const void* A, const void* Wpacked, void* Y, int64_t M, int64_t K,
+                               int64_t N, swiglu_stream_t stream) {
+  return swiglu_forward_variant(A, Wpacked, Y, M, K, N, SWIGLU_VARIANT_AUTO, stream);
+}
+
+swiglu_status_t swiglu_forward_from_host(const void* A_host, const void* Wpacked, void* Y_host,
+                                         void* A_dev, void* Y_dev, int64_t M, int64_t K,
+                                         int64_t N, swiglu_stream_t stream) {
+  swiglu_status_t st = check_forward_args(A_dev, Wpacked, Y_dev, M, K, N);
+  if (st != SWIGLU_OK) return st;
+  if (M == 0) return SWIGLU_OK;
+  if (!A_host || !Y_host) return SWIGLU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != SWIGLU_OK) return st;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(A_dev, A_host, size_t(M) * size_t(K) * 2, cudaMemcpyHostToDevice, s) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_ERR_CUDA;
+  }
+  Plan pl;
+  st = make_plan(M, N, SWIGLU_VARIANT_AUTO, d->sm_count, &pl);
+  if (st != SWIGLU_OK) return st;
+  st = launch_forward(A_dev, Wpacked, Y_dev, M, K, N, pl, *d, s);
+  if (st != SWIGLU_OK) return st;
+  if (cudaMemcpyAsync(Y_host, Y_dev, size_t(M) * size_t(N) * 2, cudaMemcpyDeviceToHost, s) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_ERR_CUDA;
+  }
+  return SWIGLU_OK;
+}
+
+swiglu_status_t swiglu_check_device_status(swiglu_stream_t stream) {
+  DeviceState* d = nullptr;
+  swiglu_status_t st = device_state(&d);
+  if (st != SWIGLU_OK) return st;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_ERR_CUDA;
+  }
+  uint32_t h[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(h, d->status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_ERR_CUDA;
+  }
+  if (h[0] == 0) return SWIGLU_OK;
+  if (std::getenv("SWIGLU_VERBOSE"))
+    std::fprintf(stderr, "libswiglu: device status %u (wait site %u, block %u, %u failures)\n",
+                 h[0], h[1], h[2], h[3]);
+  if (cudaMemset(d->status, 0, sizeof(h)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_ERR_CUDA;
+  }
+  return h[0] == 4 ? SWIGLU_ERR_TIMEOUT : SWIGLU_ERR_CUDA;
+}
+
+const char* swiglu_status_string(swiglu_status_t status) {
+  switch (status) {
+    case SWIGLU_OK: return "SWIGLU_OK";
+    case SWIGLU_ERR_INVALID_ARG: return "SWIGLU_ERR_INVALID_ARG: invalid argument";
+    case SWIGLU_ERR_UNSUPPORTED: return "SWIGLU_ERR_UNSUPPORTED: unsupported shape or device";
+    case SWIGLU_ERR_CUDA: return "SWIGLU_ERR_CUDA: CUDA call or kernel launch failed";
+    case SWIGLU_ERR_TIMEOUT: return "SWIGLU_ERR_TIMEOUT: a kernel pipeline wait timed out";
+    case SWIGLU_ERR_NO_DEVICE: return "SWIGLU_ERR_NO_DEVICE: no usable CUDA device";
+    default: return "SWIGLU_ERR_UNKNOWN";
+  }
+}
+
+swiglu_status_t swiglu_plan_string(int64_t M, int64_t K, int64_t N, int variant, char* buf,
+                                   size_t buflen) {
+  if (!buf || buflen == 0) return SWIGLU_ERR_INVALID_ARG;
+  buf[0] = '\0';
+  swiglu_status_t st = check_shape(M, K, N);
+  if (st != SWIGLU_OK) return st;
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != SWIGLU_OK) return st;
+  Plan pl;
+  st = make_plan(M < 1 ? 1 : M, N, variant, d->sm_count, &pl);
+  if (st != SWIGLU_OK) return st;
+  if (pl.variant == SWIGLU_VARIANT_SMALL_M)
+    std::snprintf(buf, buflen, "small_m mt=%d stages=%d tiles=%d grid=%d sms=%d", pl.mt,
+                  pl.stages, pl.tiles, pl.grid, d->sm_count);
+  else
+    std::snprintf(buf, buflen, "large_m bn=%d stages=%d tiles=%d grid=%d group_m=%d sms=%d",
+                  pl.bn, pl.stages, pl.tiles, pl.grid, pl.group_m, d->sm_count);
+  return SWIGLU_OK;
+}
+
+void swiglu_testing_inject_stall(int enable, uint32_t timeout_ms) {
+  g_inject.store(enable ? 1 : 0);
+  if (timeout_ms) g_timeout_ns.store(uint64_t(timeout_ms) * 1000000ull);
+}
+
+}  // extern "C"

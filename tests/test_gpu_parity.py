@@ -1,0 +1,182 @@
+"""Parity of the CUDA path with the CPU oracle (needs a GB300).
+
+Element-by-element comparison on seeded inputs at sizes the oracle finishes in
+seconds, spanning several tiles and ragged tails in M, K and N, for both
+kernels and the automatic choice. Pass rule: |y - ref| <= 1e-2 |ref| + 1e-3
+for every element; no non-finite outputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import pack_layout
+from oracle.swiglu_ref import swiglu_f64_values, f64_to_bf16_bits, swiglu_f64
+from swiglu_gated_mlp_gb300.workloads import bf16_bits, make_inputs
+
+from gpu_helpers import (check_against_oracle, run_forward, sentinel_buffer, sentinel_intact,
+                         to_dev)
+
+pytestmark = pytest.mark.gpu
+
+AUTO, LARGE, SMALL = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def native(native_lib):
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return native_lib
+
+
+# ------------------------------------------------------------------ pack ----
+
+@pytest.mark.parametrize("K,N", [(64, 128), (72, 136), (200, 264), (896, 4864), (8, 8)])
+def test_pack_is_bit_exact(native, K, N):
+    _, w1, w2 = make_inputs(1, K, N, seed=K + N)
+    w1d, w2d = to_dev(w1, w2)
+    wp = native.swiglu_pack_weights(w1d, w2d)
+    torch.cuda.synchronize()
+    want = pack_layout.pack_reference(bf16_bits(w1), bf16_bits(w2))
+    assert np.array_equal(bf16_bits(wp.cpu()), want)
+
+
+# --------------------------------------------------------------- forward ----
+
+SMALL_CASES = [
+    (1, 64, 128), (2, 72, 136), (7, 200, 264), (16, 256, 1024), (17, 128, 384),
+    (33, 520, 256), (64, 1024, 512), (100, 136, 392), (256, 192, 256), (16, 3584, 640),
+]
+
+LARGE_CASES = [
+    (1, 64, 128), (100, 200, 264), (128, 64, 128), (129, 136, 256), (300, 512, 1000),
+    (1000, 256, 512), (513, 896, 4864), (256, 3584, 1024), (384, 72, 8), (2048, 128, 2048),
+]
+
+AUTO_CASES = [(16, 3584, 1280), (64, 512, 768), (65, 512, 768), (128, 896, 4864), (1024, 1024, 1024)]
+
+
+@pytest.mark.parametrize("M,K,N", SMALL_CASES)
+def test_small_m_kernel_matches_oracle(native, M, K, N):
+    check_against_oracle(native, M, K, N, seed=M * 7 + K + N, variant=SMALL)
+
+
+@pytest.mark.parametrize("M,K,N", LARGE_CASES)
+def test_large_m_kernel_matches_oracle(native, M, K, N):
+    check_against_oracle(native, M, K, N, seed=M * 5 + K + N, variant=LARGE)
+
+
+@pytest.mark.parametrize("M,K,N", AUTO_CASES)
+def test_auto_choice_matches_oracle(native, M, K, N):
+    check_against_oracle(native, M, K, N, seed=M + K + N, variant=AUTO)
+
+
+@pytest.mark.parametrize("variant", [LARGE, SMALL])
+def test_variants_agree(native, variant):
+    # both kernels accumulate in fp32; their bf16 outputs agree within 1 ulp-ish
+    a, w1, w2 = make_inputs(48, 640, 512, seed=77)
+    y_auto, _ = run_forward(native, a, w1, w2, AUTO)
+    y_var, _ = run_forward(native, a, w1, w2, variant)
+    assert torch.allclose(y_auto.float(), y_var.float(), rtol=1e-2, atol=1e-3)
+
+
+# ------------------------------------------------------- special values ----
+
+@pytest.mark.parametrize("variant", [LARGE, SMALL])
+def test_zero_activations_give_exact_zero(native, variant):
+    _, w1, w2 = make_inputs(1, 256, 384, seed=4)
+    a = torch.zeros(40, 256, dtype=torch.bfloat16)
+    y, _ = run_forward(native, a, w1, w2, variant)
+    assert torch.count_nonzero(y.float()) == 0
+
+
+@pytest.mark.parametrize("variant", [LARGE, SMALL])
+def test_large_gate_magnitudes_stay_finite(native, variant):
+    # Gate values spread over [-240, 240]: SiLU's exp overflows for the most
+    # negative ones; the result must be the signed-zero limit, never NaN.
+    K, N, M = 64, 256, 32
+    a = torch.zeros(M, K, dtype=torch.bfloat16)
+    a[:, 0] = torch.linspace(-15, 15, M).to(torch.bfloat16)
+    w1 = torch.zeros(K, N, dtype=torch.bfloat16)
+    w1[0, :] = torch.linspace(-16, 16, N).to(torch.bfloat16)
+    w2 = torch.ones(K, N, dtype=torch.bfloat16)
+    y, _ = run_forward(native, a, w1, w2, variant)
+    assert torch.isfinite(y.float()).all()
+    ref = swiglu_f64(bf16_bits(a), bf16_bits(w1), bf16_bits(w2))
+    from oracle import compare
+    assert compare.report(bf16_bits(y), ref)["tolerance_pass"]
+
+
+@pytest.mark.parametrize("variant", [LARGE, SMALL])
+def test_identity_slice(native, variant):
+    # K = N, W1 = W2 = I  =>  Y = SiLU(A) (.) A
+    K = N = 128
+    a, _, _ = make_inputs(64, K, N, seed=31)
+    eye = torch.eye(K, dtype=torch.bfloat16)
+    y, _ = run_forward(native, a, eye, eye, variant)
+    av = a.double().numpy()
+    want = swiglu_f64_values(av, np.eye(K), np.eye(K))
+    from oracle import compare
+    assert compare.report(bf16_bits(y), want)["tolerance_pass"]
+
+
+# ------------------------------------------------- memory and streams ----
+
+@pytest.mark.parametrize("variant,M", [(LARGE, 200), (SMALL, 9), (LARGE, 5)])
+def test_writes_stay_inside_y(native, variant, M):
+    K, N, pad = 128, 392, 4096
+    a, w1, w2 = make_inputs(M, K, N, seed=8)
+    ad, w1d, w2d = to_dev(a, w1, w2)
+    wp = native.swiglu_pack_weights(w1d, w2d)
+    buf = sentinel_buffer(M * N, pad)
+    y = buf[pad:pad + M * N].view(M, N)
+    native.swiglu_forward_variant(ad, wp, N, variant, Y=y)
+    native.swiglu_check_device_status()
+    assert sentinel_intact(buf, pad)
+    ref = swiglu_f64(bf16_bits(a), bf16_bits(w1), bf16_bits(w2))
+    from oracle import compare
+    assert compare.report(bf16_bits(y.cpu()), ref)["tolerance_pass"]
+
+
+def test_runs_on_a_side_stream(native):
+    a, w1, w2 = make_inputs(96, 256, 512, seed=10)
+    ad, w1d, w2d = to_dev(a, w1, w2)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        wp = native.swiglu_pack_weights(w1d, w2d)
+        y = native.swiglu_forward(ad, wp, 512)
+    s.synchronize()
+    native.swiglu_check_device_status(stream=s)
+    ref = swiglu_f64(bf16_bits(a), bf16_bits(w1), bf16_bits(w2))
+    from oracle import compare
+    assert compare.report(bf16_bits(y.cpu()), ref)["tolerance_pass"]
+
+
+def test_repeated_calls_are_identical(native):
+    a, w1, w2 = make_inputs(300, 512, 640, seed=12)
+    ad, w1d, w2d = to_dev(a, w1, w2)
+    wp = native.swiglu_pack_weights(w1d, w2d)
+    y1 = native.swiglu_forward(ad, wp, 640).clone()
+    for _ in range(5):
+        y2 = native.swiglu_forward(ad, wp, 640)
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
+def test_forward_from_host_buffers(native):
+    M, K, N = 16, 512, 640
+    a, w1, w2 = make_inputs(M, K, N, seed=14)
+    w1d, w2d = to_dev(w1, w2)
+    wp = native.swiglu_pack_weights(w1d, w2d)
+    a_host = a.pin_memory()
+    y_host = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
+    a_dev = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
+    y_dev = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    native.swiglu_forward_from_host(a_host, wp, N, y_host, a_dev, y_dev)
+    torch.cuda.synchronize()
+    ref = swiglu_f64(bf16_bits(a), bf16_bits(w1), bf16_bits(w2))
+    from oracle import compare
+    assert compare.report(bf16_bits(y_host), ref)["tolerance_pass"]
+
+
+def test_plan_string_names_a_kernel(native):
+    assert native.swiglu_plan_string(16, 3584, 18944).startswith("small_m")
+    assert native.swiglu_plan_string(4096, 3584, 18944).startswith("large_m bn=128")
