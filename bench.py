@@ -1,0 +1,448 @@
+"""Benchmark of the fused SwiGLU projection Y = SiLU(A W1) * (A W2) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-cpu-baseline]
+
+One step = one swiglu_forward call over one batch of synthetic input (the
+packed weight is prepared once, before timing, as at model load). Prints one
+JSON line (rank 0). Metric: TFLOP/s counted as 4*M*K*N per step.
+
+* value: whole-job TFLOP/s with inputs resident in HBM; K steps timed with
+  CUDA events between barriers + synchronisations, max over ranks.
+* roofline: the fused kernel's achieved bytes/s (decode workloads, HBM bound)
+  or FLOP/s (prefill workloads, tensor bound) per launch, against the measured
+  peaks in MEASURED_PEAKS.json.
+* e2e: the same metric through swiglu_forward_from_host, with each step's
+  activations copied from pinned host memory and its output copied back.
+* cpu_baseline: the CPU oracle (float64) on a bounded sample of the workload.
+* --impl reference: the CPU oracle timed as the reference arm (the method has
+  no runnable reference implementation).
+N > 1 runs independent replicas (the op has no exchange step), one per rank.
+"""
+from __future__ import annotations
+
+import os
+
+# BLAS threads of the CPU oracle: the cores this process may run on.
+_CORES = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+os.environ.setdefault("OPENBLAS_NUM_THREADS", str(_CORES))
+os.environ.setdefault("OMP_NUM_THREADS", str(_CORES))
+
+import argparse  # noqa: E402
+import glob  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import math  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from swiglu_gated_mlp_gb300.workloads import (WORKLOADS, Workload, bf16_bits,  # noqa: E402
+                                              make_workload_inputs, sweep_32b)
+
+METRIC = "fused SwiGLU-GEMM TFLOP/s (4·M·K·N) and % of GB300 dense BF16 peak"
+DEFAULT_WORKLOAD = "qwen2.5-7b-decode-m16"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["swiglu_gated_mlp_gb300/csrc/" + f for f in
+                  ("fused_small_m.cu", "fused_large_m.cu", "ptx.cuh", "kernels.h", "swiglu_api.cu")]
+
+
+def workload_by_name(name: str) -> Workload:
+    if name in WORKLOADS:
+        return WORKLOADS[name]
+    if name.startswith("qwen2.5-32b-m"):
+        return sweep_32b(int(name.rsplit("m", 1)[1]))
+    raise SystemExit(f"unknown workload {name}; known: {sorted(WORKLOADS)}")
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured (MEASURED_PEAKS.json)"
+    return dict(FALLBACK_PEAKS), "fallback (no MEASURED_PEAKS.json)"
+
+
+def source_stamp() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary of this kernel source."""
+    stamp = source_stamp()
+    for path in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        fields = {}
+        with open(path) as f:
+            for line in f:
+                if line.startswith("bench-key "):
+                    k, _, v = line[len("bench-key "):].strip().partition("=")
+                    fields[k.strip()] = v.strip()
+        if (fields.get("kernel") == kernel and fields.get("workload") == workload
+                and fields.get("source_stamp") == stamp and "dram_bytes_per_launch" in fields):
+            return float(fields["dram_bytes_per_launch"]), os.path.relpath(path, ROOT)
+    return None, None
+
+
+# ------------------------------------------------------------ distributed ----
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(flops_per_step: int, steps: int, seconds_max: float, world: int) -> float:
+    """Whole-job TFLOP/s: all ranks' work over the slowest rank's time."""
+    return world * flops_per_step * steps / seconds_max / 1e12
+
+
+# ---------------------------------------------------------------- clocks ----
+
+CLOCK_FIELDS = ["timestamp", "clocks.sm", "clocks.max.sm", "power.draw",
+                "clocks_event_reasons.active", "clocks_event_reasons.hw_slowdown",
+                "clocks_event_reasons.hw_thermal_slowdown",
+                "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while timing runs."""
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        ident = str(device_index)
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            ident = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            pass
+        self.cmd = ["nvidia-smi", "-i", ident, "--query-gpu=" + ",".join(CLOCK_FIELDS),
+                    "--format=csv,noheader,nounits", "-lms", "100"]
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < len(CLOCK_FIELDS):
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi gave no samples"}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- our arm ----
+
+def run_ours(args, w: Workload, world: int, rank: int, local: int):
+    import swiglu_gated_mlp_gb300 as sg
+    from swiglu_gated_mlp_gb300 import build as _build
+    _build.build_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    M, K, N = w.M, w.K, w.N
+
+    a_cpu, w1_cpu, w2_cpu = make_workload_inputs(w)
+    wp0 = sg.swiglu_pack_weights(w1_cpu.to(dev), w2_cpu.to(dev))
+    torch.cuda.synchronize()
+    w_bytes = wp0.numel() * 2
+    # Inputs larger than L2 between consecutive steps: rotate copies of the
+    # packed weight (and of A and Y) so no step finds its operands in L2.
+    copies = max(2, math.ceil(3 * L2_BYTES / max(w.algorithmic_bytes, 1)))
+    copies = min(copies, 64)
+    wps = [wp0] + [wp0.clone() for _ in range(copies - 1)]
+    a0 = a_cpu.to(dev)
+    As = [a0] + [a0.clone() for _ in range(copies - 1)]
+    Ys = [torch.empty(M, N, dtype=torch.bfloat16, device=dev) for _ in range(copies)]
+    plan = sg.swiglu_plan_string(M, K, N)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        j = i % copies
+        sg.swiglu_forward(As[j], wps[j], N, Y=Ys[j], stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    sg.swiglu_check_device_status(stream=stream)
+
+    steps = args.steps
+    if steps <= 0:  # auto: about two seconds of timed work
+        t0 = time.perf_counter()
+        for i in range(20):
+            step(i)
+        torch.cuda.synchronize()
+        est = (time.perf_counter() - t0) / 20
+        steps = int(min(max(50, 2.0 / max(est, 1e-6)), 50000))
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(dev.index)
+    barrier(world)
+    torch.cuda.synchronize()
+    with sampler:
+        t_begin.record(stream)
+        for i in range(steps):
+            starts[i].record(stream)
+            step(i)
+            ends[i].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    sg.swiglu_check_device_status(stream=stream)
+    elapsed = t_begin.elapsed_time(t_end) * 1e-3
+    launch_s = [s.elapsed_time(e) * 1e-3 for s, e in zip(starts, ends)]
+    elapsed_max = max_over_ranks(elapsed, world)
+    value = aggregate(w.flops, steps, elapsed_max, world)
+    avg_launch = sum(launch_s) / len(launch_s)
+
+    peaks, peak_src = load_peaks()
+    hbm_bound = w.flops / w.algorithmic_bytes < peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    kernel = "fused_small_m_kernel" if plan.startswith("small_m") else "fused_large_m_kernel"
+    traffic, traffic_src = profiled_traffic(kernel, w.name)
+    if hbm_bound:
+        achieved = w.algorithmic_bytes / avg_launch / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": traffic, "algorithmic_bytes": w.algorithmic_bytes}
+    else:
+        achieved = w.flops / avg_launch / 1e12
+        sus = peaks.get("bf16_tflops_sustained")
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "traffic": traffic, "algorithmic_flops": w.flops,
+                "peak_sustained": sus, "frac_sustained": round(achieved / sus, 4) if sus else None}
+    roof.update({"kernel": kernel, "plan": plan, "avg_launch_us": round(avg_launch * 1e6, 3),
+                 "peak_source": peak_src + (", burst" if not hbm_bound else ", copy bandwidth"),
+                 "traffic_source": traffic_src})
+
+    # ---- end to end through the public API: host activations in, host output out
+    a_host = [a_cpu.pin_memory()] + [a_cpu.clone().pin_memory() for _ in range(min(copies, 4) - 1)]
+    y_host = [torch.empty(M, N, dtype=torch.bfloat16).pin_memory() for _ in range(len(a_host))]
+    a_dev = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+    y_dev = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    e2e_steps = steps
+
+    def e2e_step(i):
+        j = i % len(a_host)
+        sg.swiglu_forward_from_host(a_host[j], wps[i % copies], N, y_host[j], a_dev, y_dev,
+                                    stream=stream)
+
+    for i in range(max(3, args.warmup // 10)):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    barrier(world)
+    sg.swiglu_check_device_status(stream=stream)
+    e2e = {"value": round(aggregate(w.flops, e2e_steps, e2e_s, world), 3), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": 2 * M * K, "d2h_bytes_per_step": 2 * M * N,
+           "steps": e2e_steps, "api": "swiglu_forward_from_host"}
+
+    out = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(elapsed_max / steps * 1e3, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "M": M, "K": K, "N": N, "seed": w.seed,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"inputs larger than L2: {copies} rotating copies of A, packed W and Y "
+                         f"({copies * w.algorithmic_bytes / 2**20:.0f} MiB)",
+                   "note": w.note},
+        "pct_bf16_peak": round(100 * value / world / peaks["bf16_tflops"], 3),
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": steps,
+        "clocks": sampler.summary(),
+        "packed_weight_bytes": w_bytes,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
+    return out
+
+
+# ---------------------------------------------------------- oracle timing ----
+
+def _oracle_sample_call(a_bits, w1_bits, w2_bits, cols):
+    from oracle.swiglu_ref import swiglu_f64
+    return swiglu_f64(a_bits, w1_bits[:, cols], w2_bits[:, cols])
+
+
+def cpu_baseline(w: Workload, budget_s: float = 12.0, per_step_s: float | None = None):
+    """The float64 CPU oracle, as it stands, on a bounded column sample of the workload.
+
+    Rows are kept whole; a contiguous block of output columns is taken so that
+    one call costs about `per_step_s` (or the whole budget is split into
+    several calls). Returns TFLOP/s counted like the GPU metric (4*M*K*cols).
+    """
+    a, w1, w2 = make_workload_inputs(w)
+    a_bits, w1_bits, w2_bits = bf16_bits(a), bf16_bits(w1), bf16_bits(w2)
+    # calibrate on a small block
+    probe_cols = max(8, min(w.N, 256))
+    t0 = time.perf_counter()
+    _oracle_sample_call(a_bits, w1_bits, w2_bits, slice(0, probe_cols))
+    t_probe = max(time.perf_counter() - t0, 1e-4)
+    per_col = t_probe / probe_cols
+    target = per_step_s if per_step_s else min(budget_s / 4, 3.0)
+    cols = int(max(8, min(w.N, target / per_col)))
+    calls, total_t, flops = 0, 0.0, 0
+    t_start = time.perf_counter()
+    while True:
+        c0 = (calls * cols) % max(w.N - cols + 1, 1)
+        t0 = time.perf_counter()
+        _oracle_sample_call(a_bits, w1_bits, w2_bits, slice(c0, c0 + cols))
+        total_t += time.perf_counter() - t0
+        flops += 4 * w.M * w.K * cols
+        calls += 1
+        if per_step_s or time.perf_counter() - t_start > budget_s:
+            break
+    return {"value": round(flops / total_t / 1e12, 6), "unit": "TFLOP/s", "cores": _CORES,
+            "kind": "oracle",
+            "sample": f"{calls} call(s) of the float64 oracle on all {w.M} rows x {cols} of "
+                      f"{w.N} columns (K={w.K}), {total_t:.1f} s of CPU time",
+            "threads_env": os.environ.get("OPENBLAS_NUM_THREADS")}
+
+
+def run_reference(args, w: Workload, world: int, rank: int):
+    """Reference arm: the CPU oracle timed on bounded samples of the workload."""
+    if rank != 0:
+        return None
+    steps = args.steps if args.steps > 0 else 20
+    warm = max(args.warmup, 0)
+    per_step = max(0.001, min(2.0, 90.0 / (steps + warm)))
+    a, w1, w2 = make_workload_inputs(w)
+    a_bits, w1_bits, w2_bits = bf16_bits(a), bf16_bits(w1), bf16_bits(w2)
+    probe_cols = max(8, min(w.N, 256))
+    t0 = time.perf_counter()
+    _oracle_sample_call(a_bits, w1_bits, w2_bits, slice(0, probe_cols))
+    per_col = max(time.perf_counter() - t0, 1e-4) / probe_cols
+    cols = int(max(8, min(w.N, per_step / per_col)))
+    for i in range(warm):
+        _oracle_sample_call(a_bits, w1_bits, w2_bits, slice(0, cols))
+    t0 = time.perf_counter()
+    for i in range(steps):
+        c0 = (i * cols) % max(w.N - cols + 1, 1)
+        _oracle_sample_call(a_bits, w1_bits, w2_bits, slice(c0, c0 + cols))
+    t = time.perf_counter() - t0
+    value = 4 * w.M * w.K * cols * steps / t / 1e12
+    sample = (f"each step: the float64 oracle on all {w.M} rows x {cols} of {w.N} columns "
+              f"(K={w.K})")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": steps, "warmup": warm, "ms_per_step": round(t / steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "seed": w.seed,
+                   "note": "no runnable implementation accompanies the method; the CPU "
+                           "float64 oracle stands in as the reference arm"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": _CORES,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=0, help="timed steps (0: about 2 s of work)")
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = p.parse_args(argv)
+    args.warmup = max(args.warmup, 3)
+    w = workload_by_name(args.workload)
+    if args.impl == "reference":
+        # rank 0 alone runs the CPU reference; other ranks exit without work
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        out = run_reference(args, w, world, rank)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    world, rank, local = dist_setup(args.gpus)
+    out = run_ours(args, w, world, rank, local)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
