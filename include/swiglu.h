@@ -162,6 +162,34 @@ SWIGLU_API swiglu_status_t swiglu_plan_string(int64_t M, int64_t K, int64_t N, i
                                               char* buf, size_t buflen);
 
 /*
+ * Allocation-free forward for callers that cannot call cudaMalloc: code that
+ * runs while a stream is being captured into a CUDA graph (allocation is not
+ * allowed there), serving runtimes that reserve all device memory for their
+ * own pools up front, and hosts that forbid allocation after start-up. The
+ * other forward entry points allocate one small status record per device on
+ * first use; this one runs the decode (small-M) kernel with that record in a
+ * file-scope static device array of 256 bytes instead, held by every GPU that
+ * loads the library until the process exits. The paper has no counterpart:
+ * this is a deployment variant, not part of the method.
+ *
+ * Same arguments and result as swiglu_forward, for M <= 256 (larger M:
+ * UNSUPPORTED). The caller passes every input and output; the library
+ * allocates nothing (no cudaMalloc, cudaFree or allocating library call).
+ * Each call clears the shared status record on `stream` before the kernel;
+ * if `status_out` (HOST, 4 x uint32, may be NULL) is given, the record is
+ * copied there after the kernel, on `stream`: status_out[0] is 0, or 4
+ * (SWIGLU_ERR_TIMEOUT) if a pipeline wait gave up; read it after the stream
+ * synchronises (page-locked memory keeps the copy asynchronous).
+ * The first call on a device does a one-time set-up (kernel attributes and the
+ * array's device address); make that first call before any stream capture.
+ * Calls whose kernels overlap on the GPU (several streams) share the record
+ * and race on it; serialise them to get a meaningful status.
+ */
+SWIGLU_API swiglu_status_t swiglu_forward_noalloc(const void* A, const void* Wpacked, void* Y,
+                                                  int64_t M, int64_t K, int64_t N,
+                                                  uint32_t* status_out, swiglu_stream_t stream);
+
+/*
  * Testing hook for the failure path: while `enable` is non-zero, the next
  * forward launches skip one pipeline-stage fill, so a wait inside the kernel
  * runs out after `timeout_ms` milliseconds (default 1000) and the kernel exits

@@ -50,6 +50,8 @@ lib.swiglu_status_string.argtypes = [_int]
 lib.swiglu_status_string.restype = ctypes.c_char_p
 lib.swiglu_plan_string.argtypes = [_i64, _i64, _i64, _int, ctypes.c_char_p, _sz]
 lib.swiglu_plan_string.restype = _int
+lib.swiglu_forward_noalloc.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp]
+lib.swiglu_forward_noalloc.restype = _int
 lib.swiglu_testing_inject_stall.argtypes = [_int, _u32]
 lib.swiglu_testing_inject_stall.restype = None
 
@@ -157,6 +159,27 @@ def swiglu_forward_from_host(A_host: torch.Tensor, Wpacked: torch.Tensor, N: int
                                             _stream_handle(stream, A_dev.device)),
                "swiglu_forward_from_host")
     return Y_host
+
+
+def swiglu_forward_noalloc(A: torch.Tensor, Wpacked: torch.Tensor, N: int, Y: torch.Tensor,
+                           status_out=None, stream=None) -> torch.Tensor:
+    """Allocation-free decode forward (M <= 256) into a caller-provided Y.
+
+    `status_out`: optional ctypes uint32 array of 4 (host) that receives the
+    kernel's status record after the stream synchronises.
+    """
+    _dev_bf16(A, "A")
+    _dev_bf16(Wpacked, "Wpacked")
+    _dev_bf16(Y, "Y")
+    M, K = A.shape
+    if tuple(Y.shape) != (M, N):
+        raise ValueError("Y must be [M, N]")
+    ptr = ctypes.addressof(status_out) if status_out is not None else None
+    with torch.cuda.device(A.device):
+        _check(lib.swiglu_forward_noalloc(A.data_ptr(), Wpacked.data_ptr(), Y.data_ptr(), M, K, N,
+                                          ptr, _stream_handle(stream, A.device)),
+               "swiglu_forward_noalloc")
+    return Y
 
 
 def swiglu_check_device_status(stream=None, device=None) -> None:

@@ -20,6 +20,14 @@ namespace swg {
 namespace {
 
 constexpr int kWStageBytes = 2 * kPackBlockN * kBlockK * 2;  // 32 KB: 256 packed rows x 128 B
+
+// Scratch of the allocation-free entry point (swiglu_forward_noalloc): the
+// status record the kernel writes when a pipeline wait gives up, placed in a
+// file-scope device array instead of library-allocated memory. Every GPU that
+// loads the library holds these 256 bytes until the process exits; all calls
+// of that entry point on a device share them.
+static __device__ __align__(256) uint32_t g_static_scratch[kStaticScratchWords];
+
 constexpr int kMaxStages = 8;
 constexpr size_t kSmemLimit = 232448;
 constexpr int kBarBytes = 256;
@@ -199,6 +207,16 @@ size_t small_m_smem_bytes(int mt, int stages) {
 cudaError_t configure_small_m() {
   return cudaFuncSetAttribute(fused_small_m_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(kSmemLimit));
+}
+
+cudaError_t static_scratch_address(uint32_t** out) {
+  // The array's name is a host-side stand-in in host code; the device address
+  // comes from the runtime, for the current device.
+  void* ptr = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+  if (e != cudaSuccess) return e;
+  *out = static_cast<uint32_t*>(ptr);
+  return cudaSuccess;
 }
 
 cudaError_t launch_small_m(const SmallMParams& p, cudaStream_t stream) {

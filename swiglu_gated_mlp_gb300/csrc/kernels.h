@@ -48,6 +48,13 @@ int large_m_stages(int bn);
 size_t large_m_smem_bytes(int bn);
 cudaError_t launch_large_m(const LargeMParams& p, cudaStream_t stream);
 
+// Words of the static scratch array behind swiglu_forward_noalloc (256 bytes);
+// a call uses the first kStatusWords of them for its status record.
+constexpr int kStaticScratchWords = 64;
+constexpr int kStatusWords = 4;
+// Device address of that array on the current device (no allocation).
+cudaError_t static_scratch_address(uint32_t** out);
+
 int small_m_stages(int mt);
 size_t small_m_smem_bytes(int mt, int stages);
 cudaError_t launch_small_m(const SmallMParams& p, cudaStream_t stream);

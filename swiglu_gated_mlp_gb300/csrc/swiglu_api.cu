@@ -230,6 +230,64 @@ swiglu_status_t launch_forward(const void* A, const void* Wp, void* Y, int64_t M
   return SWIGLU_OK;
 }
 
+// ---- set-up of the allocation-free entry point (swiglu_forward_noalloc) ----
+// Per device: compute capability, the tensor-map encoder, the decode kernel's
+// shared-memory limit and the device address of the static scratch array. No
+// step allocates device memory.
+struct NoAllocState {
+  std::atomic<bool> ready{false};
+  swiglu_status_t init_status = SWIGLU_OK;
+  uint32_t* scratch = nullptr;
+};
+NoAllocState g_noalloc[kMaxDevices];
+
+swiglu_status_t noalloc_init(NoAllocState& s) {
+  int dev = -1, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_ERR_NO_DEVICE;
+  }
+  if (major != 10 || minor != 3) return SWIGLU_ERR_UNSUPPORTED;
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+      cudaGetLastError();
+      return SWIGLU_ERR_CUDA;
+    }
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  if (swg::configure_small_m() != cudaSuccess || swg::static_scratch_address(&s.scratch) != cudaSuccess ||
+      s.scratch == nullptr) {
+    cudaGetLastError();
+    return SWIGLU_ERR_CUDA;
+  }
+  return SWIGLU_OK;
+}
+
+swiglu_status_t noalloc_state(NoAllocState** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_ERR_NO_DEVICE;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return SWIGLU_ERR_UNSUPPORTED;
+  NoAllocState& s = g_noalloc[dev];
+  if (!s.ready.load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(g_init_mu);
+    if (!s.ready.load(std::memory_order_relaxed)) {
+      s.init_status = noalloc_init(s);
+      s.ready.store(true, std::memory_order_release);
+    }
+  }
+  *out = &s;
+  return s.init_status;
+}
+
 }  // namespace
 
 extern "C" {
@@ -365,6 +423,57 @@ swiglu_status_t swiglu_plan_string(int64_t M, int64_t K, int64_t N, int variant,
   else
     std::snprintf(buf, buflen, "large_m bn=%d stages=%d tiles=%d grid=%d group_m=%d sms=%d",
                   pl.bn, pl.stages, pl.tiles, pl.grid, pl.group_m, d->sm_count);
+  return SWIGLU_OK;
+}
+
+swiglu_status_t swiglu_forward_noalloc(const void* A, const void* Wpacked, void* Y, int64_t M,
+                                       int64_t K, int64_t N, uint32_t* status_out,
+                                       swiglu_stream_t stream) {
+  swiglu_status_t st = check_forward_args(A, Wpacked, Y, M, K, N);
+  if (st != SWIGLU_OK) return st;
+  if (M > 256) return SWIGLU_ERR_UNSUPPORTED;  // the decode kernel's limit
+  if (swg::kStatusWords > swg::kStaticScratchWords) return SWIGLU_ERR_UNSUPPORTED;
+  if (M == 0) {
+    if (status_out) std::memset(status_out, 0, swg::kStatusWords * sizeof(uint32_t));
+    return SWIGLU_OK;
+  }
+  NoAllocState* s = nullptr;
+  st = noalloc_state(&s);
+  if (st != SWIGLU_OK) return st;
+  Plan pl;
+  st = make_plan(M, N, SWIGLU_VARIANT_SMALL_M, 0, &pl);
+  if (st != SWIGLU_OK) return st;
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  // The shared array keeps the previous call's record: the status must start at zero.
+  if (cudaMemsetAsync(s->scratch, 0, swg::kStatusWords * sizeof(uint32_t), cs) != cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_ERR_CUDA;
+  }
+  const int64_t np = padded_n(N);
+  swg::SmallMParams p{};
+  if (!encode_2d(&p.tmap_x, A, K, M, K * 2, swg::kBlockK, pl.mt, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&p.tmap_w, Wpacked, K, 2 * np, K * 2, swg::kBlockK, 2 * swg::kPackBlockN,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return SWIGLU_ERR_CUDA;
+  p.y = Y;
+  p.M = static_cast<int>(M);
+  p.K = static_cast<int>(K);
+  p.N = static_cast<int>(N);
+  p.mt = pl.mt;
+  p.stages = pl.stages;
+  p.grid = pl.grid;
+  p.status = s->scratch;
+  p.timeout_ns = g_timeout_ns.load();
+  p.inject_stall = g_inject.load();
+  if (swg::launch_small_m(p, cs) != cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_ERR_CUDA;
+  }
+  if (status_out && cudaMemcpyAsync(status_out, s->scratch, swg::kStatusWords * sizeof(uint32_t),
+                                    cudaMemcpyDeviceToHost, cs) != cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_ERR_CUDA;
+  }
   return SWIGLU_OK;
 }
 
