@@ -71,8 +71,9 @@ typedef enum {
 
 /*
  * Size in bytes of the packed weight for a K x N gate/up pair:
- * 2 (matrices) * Np * K * 2 (bytes), Np = N rounded up to a multiple of 128.
- * Returns 0 if K <= 0, N <= 0 or the size overflows.
+ * 2 (matrices) * Np * Kp * 2 (bytes), Np = N rounded up to a multiple of 128,
+ * Kp = K rounded up to a multiple of 64.
+ * Returns 0 if K <= 0, N <= 0 or a size is beyond the limits below.
  */
 SWIGLU_API size_t swiglu_packed_weight_bytes(int64_t K, int64_t N);
 
@@ -83,12 +84,13 @@ SWIGLU_API size_t swiglu_packed_weight_bytes(int64_t K, int64_t N);
  * and Up columns come out of one GEMM ("Tile-Level Activation Overlap for
  * Efficient LLM Inference", gist.science, section "Methodology / Kernel-2":
  * W_fused, even columns Gate, odd columns Up). This library interleaves blocks
- * of 128 columns instead of single columns and stores each column
- * K-contiguous:
- *   Wp viewed as bf16 [Np/128][256][K]:
- *     Wp[j][i][k]       = W1[k][j*128 + i]   (i < 128, gate)
- *     Wp[j][128 + i][k] = W2[k][j*128 + i]   (i < 128, up)
- *   and 0 for columns j*128 + i >= N.
+ * of 128 columns instead of single columns, and stores each (column block,
+ * 64-deep K slice) tile contiguously:
+ *   Wp viewed as bf16 [Np/128][Kp/64][256][64]:
+ *     Wp[j][b][i][t]       = W1[64b + t][128j + i]   (i < 128, gate)
+ *     Wp[j][b][128 + i][t] = W2[64b + t][128j + i]   (i < 128, up)
+ *   and 0 where 128j + i >= N or 64b + t >= K.
+ * Each 32 KB tile is one load of the kernels' pipeline, one contiguous span.
  *
  * W1, W2: device, [K, N] bf16 row-major. Wpacked: device, at least
  * swiglu_packed_weight_bytes(K, N) bytes, must not overlap W1 or W2.

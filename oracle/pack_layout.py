@@ -6,14 +6,15 @@ The pages fuse W1 and W2 into one K x 2N weight so that one GEMM produces
 matching Gate and Up columns side by side ("Tile-Level Activation Overlap for
 Efficient LLM Inference", gist.science technical summary, section
 "Methodology / Kernel-2": W_fused with interleaved columns, even = Gate,
-odd = Up). This library interleaves by blocks instead of single columns, and
-stores the result K-contiguous (each packed row is one weight column):
+odd = Up). This library interleaves by blocks instead of single columns and
+stores each (column block, 64-deep K slice) tile contiguously:
 
 * NB = 128 columns per block; N is zero-padded to Np = ceil(N / 128) * 128.
-* Packed array P has shape [Np / 128, 256, K] (bf16), i.e. [2 * Np, K]:
-  P[j, i, k]       = W1[k, j * 128 + i]   for i in [0, 128)   (gate rows)
-  P[j, 128 + i, k] = W2[k, j * 128 + i]   for i in [0, 128)   (up rows)
-  and 0 where j * 128 + i >= N.
+* KB = 64 K-values per slice; K is zero-padded to Kp = ceil(K / 64) * 64.
+* Packed array P has shape [Np / 128, Kp / 64, 256, 64] (bf16):
+  P[j, b, i, t]       = W1[64 b + t, 128 j + i]   for i in [0, 128)   (gate)
+  P[j, b, 128 + i, t] = W2[64 b + t, 128 j + i]   for i in [0, 128)   (up)
+  and 0 where 128 j + i >= N or 64 b + t >= K.
 
 The layout only moves bits; results do not depend on it. This module is the
 byte-level specification the CUDA pack kernel is checked against.
@@ -23,6 +24,7 @@ from __future__ import annotations
 import numpy as np
 
 PACK_BLOCK_N = 128
+PACK_BLOCK_K = 64
 
 
 def padded_n(n: int) -> int:
@@ -30,27 +32,39 @@ def padded_n(n: int) -> int:
     return -(-n // PACK_BLOCK_N) * PACK_BLOCK_N
 
 
+def padded_k(k: int) -> int:
+    """K rounded up to a whole number of 64-deep slices."""
+    return -(-k // PACK_BLOCK_K) * PACK_BLOCK_K
+
+
 def pack_reference(w1_bits: np.ndarray, w2_bits: np.ndarray) -> np.ndarray:
-    """Packed array [2 * Np, K] (uint16 bf16 bits) from W1, W2 [K, N] (uint16)."""
+    """Packed array [Np/128, Kp/64, 256, 64] (uint16 bf16 bits) from W1, W2 [K, N]."""
     w1_bits = np.asarray(w1_bits, dtype=np.uint16)
     w2_bits = np.asarray(w2_bits, dtype=np.uint16)
     k_dim, n_dim = w1_bits.shape
-    n_pad = padded_n(n_dim)
-    out = np.zeros((n_pad // PACK_BLOCK_N, 2 * PACK_BLOCK_N, k_dim), dtype=np.uint16)
-    for j in range(n_pad // PACK_BLOCK_N):
-        for i in range(PACK_BLOCK_N):
-            n = j * PACK_BLOCK_N + i
-            if n < n_dim:
-                out[j, i, :] = w1_bits[:, n]
-                out[j, PACK_BLOCK_N + i, :] = w2_bits[:, n]
-    return out.reshape(2 * n_pad, k_dim)
+    n_blocks = padded_n(n_dim) // PACK_BLOCK_N
+    k_slices = padded_k(k_dim) // PACK_BLOCK_K
+    out = np.zeros((n_blocks, k_slices, 2 * PACK_BLOCK_N, PACK_BLOCK_K), dtype=np.uint16)
+    for j in range(n_blocks):
+        n0 = j * PACK_BLOCK_N
+        cols = min(PACK_BLOCK_N, n_dim - n0)          # real columns in this block
+        for b in range(k_slices):
+            k0 = b * PACK_BLOCK_K
+            depth = min(PACK_BLOCK_K, k_dim - k0)     # real K values in this slice
+            # row i of the tile is weight column n0 + i, over k0 .. k0 + depth
+            out[j, b, :cols, :depth] = w1_bits[k0:k0 + depth, n0:n0 + cols].T
+            out[j, b, PACK_BLOCK_N:PACK_BLOCK_N + cols, :depth] = \
+                w2_bits[k0:k0 + depth, n0:n0 + cols].T
+    return out
 
 
-def unpack_reference(packed: np.ndarray, n_dim: int):
+def unpack_reference(packed: np.ndarray, k_dim: int, n_dim: int):
     """Inverse of ``pack_reference``: (W1, W2) as [K, N] uint16 arrays."""
-    packed = np.asarray(packed, dtype=np.uint16)
-    two_np, k_dim = packed.shape
-    blocks = packed.reshape(two_np // (2 * PACK_BLOCK_N), 2 * PACK_BLOCK_N, k_dim)
-    gate = blocks[:, :PACK_BLOCK_N, :].reshape(-1, k_dim)[:n_dim]  # [N, K]
-    up = blocks[:, PACK_BLOCK_N:, :].reshape(-1, k_dim)[:n_dim]
-    return np.ascontiguousarray(gate.T), np.ascontiguousarray(up.T)
+    n_blocks = padded_n(n_dim) // PACK_BLOCK_N
+    k_slices = padded_k(k_dim) // PACK_BLOCK_K
+    p = np.asarray(packed, dtype=np.uint16).reshape(n_blocks, k_slices, 2 * PACK_BLOCK_N,
+                                                    PACK_BLOCK_K)
+    # [j, b, i, t] -> column 128 j + i, row 64 b + t
+    gate = p[:, :, :PACK_BLOCK_N, :].transpose(1, 3, 0, 2).reshape(k_slices * PACK_BLOCK_K, -1)
+    up = p[:, :, PACK_BLOCK_N:, :].transpose(1, 3, 0, 2).reshape(k_slices * PACK_BLOCK_K, -1)
+    return (np.ascontiguousarray(gate[:k_dim, :n_dim]), np.ascontiguousarray(up[:k_dim, :n_dim]))

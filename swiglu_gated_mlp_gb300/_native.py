@@ -96,14 +96,15 @@ def swiglu_packed_weight_bytes(K: int, N: int) -> int:
 
 def swiglu_pack_weights(W1: torch.Tensor, W2: torch.Tensor, Wpacked: torch.Tensor | None = None,
                         stream=None) -> torch.Tensor:
-    """Packed gate/up weight (bf16 [2*Np, K]) from W1, W2 [K, N] (bf16, CUDA)."""
+    """Packed gate/up weight (flat bf16 buffer) from W1, W2 [K, N] (bf16, CUDA)."""
     _dev_bf16(W1, "W1")
     _dev_bf16(W2, "W2")
     if W1.dim() != 2 or W1.shape != W2.shape:
         raise ValueError("W1 and W2 must both be [K, N]")
     K, N = W1.shape
-    if Wpacked is None:
-        Wpacked = torch.empty((2 * padded_n(N), K), dtype=torch.bfloat16, device=W1.device)
+    if Wpacked is None:  # opaque buffer of swiglu_packed_weight_bytes(K, N) bytes
+        Wpacked = torch.empty(swiglu_packed_weight_bytes(K, N) // 2, dtype=torch.bfloat16,
+                              device=W1.device)
     _dev_bf16(Wpacked, "Wpacked")
     if Wpacked.numel() * 2 < swiglu_packed_weight_bytes(K, N):
         raise ValueError("Wpacked is too small")

@@ -122,8 +122,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, mb, nb);
         const int m0 = mb * kTileM;
         const int col0 = nb * BN;
-        // first packed row of this tile's gate columns; the up rows follow 128 later
-        const int wrow = (col0 / kPackBlockN) * (2 * kPackBlockN) + (col0 % kPackBlockN);
+        // packed tile index of (column block, K slice 0), and this tile's gate rows
+        // inside the 256-row tile; the matching up rows follow 128 later
+        const int wtile = (col0 / kPackBlockN) * num_kb;
+        const int wrow = col0 % kPackBlockN;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(empty0 + 8u * s, ph ^ 1u, wc, kSiteProducerEmpty)) {
             ok = false;
@@ -136,9 +138,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int k0 = kb * kBlockK;
             mbar_arrive_expect_tx(fb, C::kStageBytes);
             tma_load_2d(sA + s * C::kABytes, &p.tmap_a, fb, k0, m0);
-            tma_load_2d(sB + s * C::kBBytes, &p.tmap_w, fb, k0, wrow);
-            tma_load_2d(sB + s * C::kBBytes + BN * kBlockK * 2, &p.tmap_w, fb, k0,
-                        wrow + kPackBlockN);
+            tma_load_3d(sB + s * C::kBBytes, &p.tmap_w, fb, 0, wrow, wtile + kb);
+            tma_load_3d(sB + s * C::kBBytes + BN * kBlockK * 2, &p.tmap_w, fb, 0,
+                        wrow + kPackBlockN, wtile + kb);
             filled |= 1u << s;
             fill_ph = (fill_ph & ~(1u << s)) | (ph << s);
           }

@@ -5,8 +5,9 @@
 // fills the SMs ("Tile-Level Activation Overlap for Efficient LLM Inference",
 // gist.science, section "Methodology / Kernel-2", Optimization). Here the
 // operands are swapped instead: each CTA owns one 128-column block of the
-// packed weight (128 gate rows + 128 up rows, K-contiguous) and streams it
-// through a deep TMA ring; the weight rows are the MMA's M side (128) and the
+// packed weight (per 64-deep K slice, 128 gate rows + 128 up rows stored as
+// one contiguous 32 KB tile) and streams it through a deep TMA ring, one tile
+// per stage; the weight rows are the MMA's M side (128) and the
 // tokens its N side (mt = M rounded up to 16), so
 //   Gate^T[128 x mt] = W1_block^T * A^T   and   Up^T likewise,
 // two tcgen05.mma per K step into two fp32 TMEM accumulators. The epilogue
@@ -85,7 +86,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();  // weights: read once
       const uint64_t pol_x = policy_evict_last();   // activations: re-read by every CTA
-      const int wrow = nblk * 2 * kPackBlockN;
+      const int wtile = nblk * num_kb;  // packed tile index of (this column block, K slice 0)
       int s = 0;
       uint32_t ph = 0;
       uint32_t filled = 0, fill_ph = 0;
@@ -99,7 +100,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sw = s0 + s * stage_bytes;
           const int k0 = kb * kBlockK;
           mbar_arrive_expect_tx(fb, stage_bytes);
-          tma_load_2d_hint(sw, &p.tmap_w, fb, k0, wrow, pol_w);
+          tma_load_3d_hint(sw, &p.tmap_w, fb, 0, 0, wtile + kb, pol_w);  // one contiguous 32 KB tile
           tma_load_2d_hint(sw + kWStageBytes, &p.tmap_x, fb, k0, 0, pol_x);
           filled |= 1u << s;
           fill_ph = (fill_ph & ~(1u << s)) | (ph << s);

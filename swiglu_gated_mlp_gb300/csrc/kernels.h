@@ -16,7 +16,7 @@ constexpr int kThreads = 192;     // 6 warps: TMA producer, MMA issuer, 4 epilog
 
 struct LargeMParams {
   CUtensorMap tmap_a;  // A  [M, K]       box {64, 128}, 128-B swizzle
-  CUtensorMap tmap_w;  // Wp [2*Np, K]    box {64, bn},  128-B swizzle
+  CUtensorMap tmap_w;  // Wp {64, 256, tiles} box {64, bn, 1}, 128-B swizzle
   CUtensorMap tmap_y;  // Y  [M, N]       box {32, 32},  64-B swizzle (store)
   int M, K, N;
   int tiles_m, tiles_n, group_m;
@@ -29,7 +29,7 @@ struct LargeMParams {
 
 struct SmallMParams {
   CUtensorMap tmap_x;  // A  [M, K]     box {64, mt}, 128-B swizzle
-  CUtensorMap tmap_w;  // Wp [2*Np, K]  box {64, 256}, 128-B swizzle
+  CUtensorMap tmap_w;  // Wp {64, 256, tiles} box {64, 256, 1}, 128-B swizzle
   void* y;             // Y  [M, N] bf16
   int M, K, N;
   int mt;      // tokens rounded up to a multiple of 16 (MMA N), <= 256

@@ -56,6 +56,8 @@ int64_t padded_n(int64_t n) {
   return (n + swg::kPackBlockN - 1) / swg::kPackBlockN * swg::kPackBlockN;
 }
 
+int64_t k_slices(int64_t k) { return (k + swg::kBlockK - 1) / swg::kBlockK; }
+
 swiglu_status_t init_device(int dev, DeviceState& d) {
   int major = 0, minor = 0;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -117,12 +119,28 @@ bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t oute
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The packed weight as a 3-D tensor {64 K values, 256 rows, tiles}: every tile
+// (one 128-column block x one 64-deep K slice, gate rows then up rows) is a
+// contiguous 32 KB span; boxes of {64, rows, 1} are taken from one tile.
+bool encode_packed_w(CUtensorMap* map, const void* base, int64_t K, int64_t N, uint32_t rows) {
+  const int64_t tiles = (padded_n(N) / swg::kPackBlockN) * k_slices(K);
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(swg::kBlockK), 2u * swg::kPackBlockN,
+                        static_cast<cuuint64_t>(tiles)};
+  cuuint64_t strides[2] = {swg::kBlockK * 2, 2u * swg::kPackBlockN * swg::kBlockK * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(swg::kBlockK), rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct Plan {
   int variant = SWIGLU_VARIANT_AUTO;
   int bn = 0, stages = 0, tiles_m = 0, tiles_n = 0, group_m = 0, tiles = 0, grid = 0, mt = 0;
 };
 
-swiglu_status_t make_plan(int64_t M, int64_t N, int variant, int sm_count, Plan* pl) {
+swiglu_status_t make_plan(int64_t M, int64_t K, int64_t N, int variant, int sm_count, Plan* pl) {
   if (variant != SWIGLU_VARIANT_AUTO && variant != SWIGLU_VARIANT_LARGE_M &&
       variant != SWIGLU_VARIANT_SMALL_M)
     return SWIGLU_ERR_INVALID_ARG;
@@ -152,7 +170,13 @@ swiglu_status_t make_plan(int64_t M, int64_t N, int variant, int sm_count, Plan*
   pl->stages = swg::large_m_stages(bn);
   pl->tiles_m = static_cast<int>(tiles_m);
   pl->tiles_n = static_cast<int>(np / bn);
-  pl->group_m = static_cast<int>(tiles_m < 16 ? tiles_m : 16);
+  // Row tiles per group: as many as keep the group's A rows within about a
+  // third of L2 (so W is read from HBM once per group, ideally once).
+  const int64_t a_tile_bytes = int64_t(swg::kTileM) * K * 2;
+  int64_t group = (48ll << 20) / (a_tile_bytes > 0 ? a_tile_bytes : 1);
+  if (group < 1) group = 1;
+  if (group > tiles_m) group = tiles_m;
+  pl->group_m = static_cast<int>(group);
   pl->tiles = static_cast<int>(tiles);
   pl->grid = static_cast<int>(tiles < sm_count ? tiles : sm_count);
   return SWIGLU_OK;
@@ -180,7 +204,6 @@ swiglu_status_t check_forward_args(const void* A, const void* Wp, const void* Y,
 
 swiglu_status_t launch_forward(const void* A, const void* Wp, void* Y, int64_t M, int64_t K,
                                int64_t N, const Plan& pl, DeviceState& d, cudaStream_t stream) {
-  const int64_t np = padded_n(N);
   const uint64_t timeout = g_timeout_ns.load();
   const int inject = g_inject.load();
   cudaError_t err;
@@ -188,8 +211,7 @@ swiglu_status_t launch_forward(const void* A, const void* Wp, void* Y, int64_t M
     swg::SmallMParams p{};
     if (!encode_2d(&p.tmap_x, A, K, M, K * 2, swg::kBlockK, pl.mt,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&p.tmap_w, Wp, K, 2 * np, K * 2, swg::kBlockK, 2 * swg::kPackBlockN,
-                   CU_TENSOR_MAP_SWIZZLE_128B))
+        !encode_packed_w(&p.tmap_w, Wp, K, N, 2 * swg::kPackBlockN))
       return SWIGLU_ERR_CUDA;
     p.y = Y;
     p.M = static_cast<int>(M);
@@ -206,8 +228,7 @@ swiglu_status_t launch_forward(const void* A, const void* Wp, void* Y, int64_t M
     swg::LargeMParams p{};
     if (!encode_2d(&p.tmap_a, A, K, M, K * 2, swg::kBlockK, swg::kTileM,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&p.tmap_w, Wp, K, 2 * np, K * 2, swg::kBlockK, pl.bn,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_packed_w(&p.tmap_w, Wp, K, N, pl.bn) ||
         !encode_2d(&p.tmap_y, Y, N, M, N * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
       return SWIGLU_ERR_CUDA;
     p.M = static_cast<int>(M);
@@ -294,7 +315,7 @@ extern "C" {
 
 size_t swiglu_packed_weight_bytes(int64_t K, int64_t N) {
   if (K <= 0 || N <= 0 || K > kMaxKN || N > kMaxKN) return 0;
-  return size_t(2) * size_t(padded_n(N)) * size_t(K) * 2;
+  return size_t(2) * size_t(padded_n(N)) * size_t(k_slices(K) * swg::kBlockK) * 2;
 }
 
 swiglu_status_t swiglu_pack_weights(const void* W1, const void* W2, void* Wpacked, int64_t K,
@@ -330,7 +351,7 @@ swiglu_status_t swiglu_forward_variant(const void* A, const void* Wpacked, void*
   st = device_state(&d);
   if (st != SWIGLU_OK) return st;
   Plan pl;
-  st = make_plan(M, N, variant, d->sm_count, &pl);
+  st = make_plan(M, K, N, variant, d->sm_count, &pl);
   if (st != SWIGLU_OK) return st;
   return launch_forward(A, Wpacked, Y, M, K, N, pl, *d, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -357,7 +378,7 @@ swiglu_status_t swiglu_forward_from_host(const void* A_host, const void* Wpacked
     return SWIGLU_ERR_CUDA;
   }
   Plan pl;
-  st = make_plan(M, N, SWIGLU_VARIANT_AUTO, d->sm_count, &pl);
+  st = make_plan(M, K, N, SWIGLU_VARIANT_AUTO, d->sm_count, &pl);
   if (st != SWIGLU_OK) return st;
   st = launch_forward(A_dev, Wpacked, Y_dev, M, K, N, pl, *d, s);
   if (st != SWIGLU_OK) return st;
@@ -415,7 +436,7 @@ swiglu_status_t swiglu_plan_string(int64_t M, int64_t K, int64_t N, int variant,
   st = device_state(&d);
   if (st != SWIGLU_OK) return st;
   Plan pl;
-  st = make_plan(M < 1 ? 1 : M, N, variant, d->sm_count, &pl);
+  st = make_plan(M < 1 ? 1 : M, K, N, variant, d->sm_count, &pl);
   if (st != SWIGLU_OK) return st;
   if (pl.variant == SWIGLU_VARIANT_SMALL_M)
     std::snprintf(buf, buflen, "small_m mt=%d stages=%d tiles=%d grid=%d sms=%d", pl.mt,
@@ -441,7 +462,7 @@ swiglu_status_t swiglu_forward_noalloc(const void* A, const void* Wpacked, void*
   st = noalloc_state(&s);
   if (st != SWIGLU_OK) return st;
   Plan pl;
-  st = make_plan(M, N, SWIGLU_VARIANT_SMALL_M, 0, &pl);
+  st = make_plan(M, K, N, SWIGLU_VARIANT_SMALL_M, 0, &pl);
   if (st != SWIGLU_OK) return st;
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   // The shared array keeps the previous call's record: the status must start at zero.
@@ -449,11 +470,9 @@ swiglu_status_t swiglu_forward_noalloc(const void* A, const void* Wpacked, void*
     cudaGetLastError();
     return SWIGLU_ERR_CUDA;
   }
-  const int64_t np = padded_n(N);
   swg::SmallMParams p{};
   if (!encode_2d(&p.tmap_x, A, K, M, K * 2, swg::kBlockK, pl.mt, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&p.tmap_w, Wpacked, K, 2 * np, K * 2, swg::kBlockK, 2 * swg::kPackBlockN,
-                 CU_TENSOR_MAP_SWIZZLE_128B))
+      !encode_packed_w(&p.tmap_w, Wpacked, K, N, 2 * swg::kPackBlockN))
     return SWIGLU_ERR_CUDA;
   p.y = Y;
   p.M = static_cast<int>(M);

@@ -36,7 +36,9 @@ def test_pack_is_bit_exact(native, K, N):
     wp = native.swiglu_pack_weights(w1d, w2d)
     torch.cuda.synchronize()
     want = pack_layout.pack_reference(bf16_bits(w1), bf16_bits(w2))
-    assert np.array_equal(bf16_bits(wp.cpu()), want)
+    got = bf16_bits(wp.cpu()).reshape(-1)
+    assert got.size * 2 == native.swiglu_packed_weight_bytes(K, N)
+    assert np.array_equal(got, want.reshape(-1))
 
 
 # --------------------------------------------------------------- forward ----

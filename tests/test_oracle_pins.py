@@ -265,20 +265,38 @@ def test_tolerance_rule_boundaries():
 # ------------------------------------------------------ packed layout ----
 
 def test_pack_layout_indices_and_padding():
-    _, w1, w2 = make_inputs(1, 24, 200, seed=21)
+    _, w1, w2 = make_inputs(1, 100, 200, seed=21)
     w1b, w2b = bf16_bits(w1), bf16_bits(w2)
     p = pack_layout.pack_reference(w1b, w2b)
-    assert p.shape == (2 * 256, 24)
-    blocks = p.reshape(2, 256, 24)
+    assert p.shape == (2, 2, 256, 64)      # Np = 256, Kp = 128
     for n in (0, 1, 127, 128, 150, 199):
         j, i = divmod(n, 128)
-        assert np.array_equal(blocks[j, i], w1b[:, n])
-        assert np.array_equal(blocks[j, 128 + i], w2b[:, n])
-    assert not blocks[1, 72:128].any() and not blocks[1, 128 + 72:].any()
+        for k in (0, 5, 63, 64, 99):
+            b, t = divmod(k, 64)
+            assert p[j, b, i, t] == w1b[k, n]
+            assert p[j, b, 128 + i, t] == w2b[k, n]
+    assert not p[1, :, 72:128].any() and not p[1, :, 128 + 72:].any()   # columns >= N
+    assert not p[:, 1, :, 36:].any()                                    # K values >= K
 
 
 def test_pack_layout_round_trip():
     _, w1, w2 = make_inputs(1, 40, 264, seed=22)
     w1b, w2b = bf16_bits(w1), bf16_bits(w2)
-    u1, u2 = pack_layout.unpack_reference(pack_layout.pack_reference(w1b, w2b), 264)
+    u1, u2 = pack_layout.unpack_reference(pack_layout.pack_reference(w1b, w2b), 40, 264)
     assert np.array_equal(u1, w1b) and np.array_equal(u2, w2b)
+
+
+def test_pack_layout_matches_elementwise_definition():
+    # the slicing in pack_reference against the definition, element by element
+    _, w1, w2 = make_inputs(1, 72, 136, seed=23)
+    w1b, w2b = bf16_bits(w1), bf16_bits(w2)
+    p = pack_layout.pack_reference(w1b, w2b)
+    for j in range(p.shape[0]):
+        for b in range(p.shape[1]):
+            for i in range(256):
+                n = 128 * j + (i % 128)
+                for t in range(64):
+                    k = 64 * b + t
+                    src = w1b if i < 128 else w2b
+                    want = src[k, n] if (k < 72 and n < 136) else 0
+                    assert p[j, b, i, t] == want
