@@ -108,6 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  pdl_wait();  // the set-up above overlaps the previous grid; memory traffic starts here
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer -----
@@ -150,6 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      pdl_launch_dependents();
       // Copies still in flight must land before the CTA may exit.
       for (int i = 0; i < C::kStages; ++i)
         if (filled & (1u << i)) mbar_wait_drain(full0 + 8u * i, (fill_ph >> i) & 1u, wc);
@@ -276,8 +278,18 @@ cudaError_t configure_bn() {
 
 template <int BN>
 cudaError_t launch_bn(const LargeMParams& p, cudaStream_t stream) {
-  fused_large_m_kernel<BN><<<p.grid, kThreads, LargeCfg<BN>::kSmem, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = LargeCfg<BN>::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, fused_large_m_kernel<BN>, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

@@ -80,6 +80,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  pdl_wait();  // the set-up above overlaps the previous grid; memory traffic starts here
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer -----
@@ -110,6 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ph ^= 1u;
         }
       }
+      pdl_launch_dependents();
       for (int i = 0; i < stages; ++i)
         if (filled & (1u << i)) mbar_wait_drain(full0 + 8u * i, (fill_ph >> i) & 1u, wc);
     }
@@ -193,10 +195,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-int small_m_stages(int mt) {
+int small_m_stages(int mt, int ctas_per_sm) {
+  // Shared memory per SM is 228 KB, of which 1 KB per resident CTA is reserved.
+  const size_t per_cta = ctas_per_sm <= 1 ? kSmemLimit : (233472 - 2048) / 2;
   const size_t stage = kWStageBytes + size_t(mt) * kBlockK * 2;
-  const size_t avail = kSmemLimit - 1024 - kBarBytes;
-  size_t s = avail / stage;
+  size_t s = (per_cta - 1024 - kBarBytes) / stage;
   if (s > kMaxStages) s = kMaxStages;
   return static_cast<int>(s);
 }
@@ -206,8 +209,13 @@ size_t small_m_smem_bytes(int mt, int stages) {
 }
 
 cudaError_t configure_small_m() {
-  return cudaFuncSetAttribute(fused_small_m_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(kSmemLimit));
+  cudaError_t e = cudaFuncSetAttribute(fused_small_m_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemLimit));
+  if (e == cudaSuccess)  // all of the unified L1/shared array as shared memory (2 CTAs may share an SM)
+    e = cudaFuncSetAttribute(fused_small_m_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             100);
+  return e;
 }
 
 cudaError_t static_scratch_address(uint32_t** out) {
@@ -223,8 +231,18 @@ cudaError_t static_scratch_address(uint32_t** out) {
 cudaError_t launch_small_m(const SmallMParams& p, cudaStream_t stream) {
   if (p.stages < 2 || p.stages > kMaxStages || p.mt < 16 || p.mt > 256 || (p.mt % 16) != 0)
     return cudaErrorInvalidValue;
-  fused_small_m_kernel<<<p.grid, kThreads, small_m_smem_bytes(p.mt, p.stages), stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = small_m_smem_bytes(p.mt, p.stages);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, fused_small_m_kernel, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace swg

@@ -55,7 +55,13 @@ constexpr int kStatusWords = 4;
 // Device address of that array on the current device (no allocation).
 cudaError_t static_scratch_address(uint32_t** out);
 
-int small_m_stages(int mt);
+// Pipeline depth of the decode kernel when `ctas_per_sm` CTAs share an SM.
+int small_m_stages(int mt, int ctas_per_sm);
+
+// Programmatic dependent launch for the fused kernels (on unless the
+// environment sets SWIGLU_PDL=0): a launch may begin while the previous grid
+// in the stream drains; the kernel waits for it before touching memory.
+bool pdl_enabled();
 size_t small_m_smem_bytes(int mt, int stages);
 cudaError_t launch_small_m(const SmallMParams& p, cudaStream_t stream);
 

@@ -45,6 +45,17 @@ int64_t small_m_max() {
   return v;
 }
 
+}  // namespace
+
+namespace swg {
+bool pdl_enabled() {
+  static const bool on = env_int("SWIGLU_PDL", 1) != 0;
+  return on;
+}
+}  // namespace swg
+
+namespace {
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
@@ -151,8 +162,13 @@ swiglu_status_t make_plan(int64_t M, int64_t K, int64_t N, int variant, int sm_c
   if (variant == SWIGLU_VARIANT_SMALL_M) {
     if (M > 256) return SWIGLU_ERR_UNSUPPORTED;
     pl->mt = static_cast<int>((M + 15) / 16 * 16);
-    pl->stages = swg::small_m_stages(pl->mt);
     pl->tiles = static_cast<int>(np / swg::kPackBlockN);
+    // One CTA per SM with the deepest ring, unless there are more column blocks
+    // than SMs: then two CTAs per SM (3+ stages each) keep the whole grid
+    // resident instead of running a second, partial wave.
+    pl->stages = swg::small_m_stages(pl->mt, 1);
+    if (sm_count > 0 && pl->tiles > sm_count && swg::small_m_stages(pl->mt, 2) >= 3)
+      pl->stages = swg::small_m_stages(pl->mt, 2);
     pl->grid = pl->tiles;
     return SWIGLU_OK;
   }
