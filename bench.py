@@ -328,9 +328,68 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
         "clocks": sampler.summary(),
         "packed_weight_bytes": w_bytes,
     }
+    if args.compare_unfused:
+        out["unfused"] = unfused_comparison(w, As, w1_cpu.to(dev), w2_cpu.to(dev), copies, steps,
+                                            elapsed / steps, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
     return out
+
+
+# ------------------------------------------------------ unfused comparator ----
+
+def unfused_comparison(w: Workload, As, w1, w2, copies: int, steps: int, fused_s: float, peaks):
+    """The unfused path the pages compare against, timed on the same GPU.
+
+    PyTorch eager: two cuBLAS GEMMs that write bf16 Gate and Up to HBM, then
+    SiLU and the product as separate kernels ("Tile-Level Activation Overlap
+    for Efficient LLM Inference", gist.science, sections "Problem Statement"
+    and "Results": speedup over PyTorch eager, fusion efficiency, arithmetic
+    intensity). Timed like the fused path: rotating inputs, CUDA events over
+    the region. Derived metrics follow the pages' model, in which fusion
+    removes four intermediate HBM operations (write and read of Gate and Up,
+    8*M*N bytes): theoretical speedup = t_unfused / (t_unfused - 8MN / HBM
+    peak); fusion efficiency = actual speedup / theoretical speedup.
+    """
+    M, K, N = w.M, w.K, w.N
+    n = max(3, min(steps, int(2.0 / max(fused_s * 2, 1e-6))))
+
+    # the same rotation of inputs larger than L2 as the fused path
+    W1s = [w1] + [w1.clone() for _ in range(copies - 1)]
+    W2s = [w2] + [w2.clone() for _ in range(copies - 1)]
+
+    def step(i):
+        j = i % copies
+        g = As[j] @ W1s[j]
+        u = As[j] @ W2s[j]
+        return torch.nn.functional.silu(g) * u
+
+    for i in range(5):
+        step(i)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(n):
+        step(i)
+    t1.record()
+    torch.cuda.synchronize()
+    t_unf = t0.elapsed_time(t1) * 1e-3 / n
+    extra = 8 * M * N
+    t_theory = max(t_unf - extra / (peaks["hbm_gbs"] * 1e9), 1e-12)
+    speedup = t_unf / fused_s
+    theoretical = t_unf / t_theory
+    ai_fused = w.flops / w.algorithmic_bytes
+    ai_unfused = w.flops / (w.algorithmic_bytes + 2 * M * K + extra)  # A read by both GEMMs
+    return {"impl": "torch eager: cuBLAS GEMM x2 (bf16 Gate, Up in HBM) + silu + mul",
+            "steps": n, "us_per_step": round(t_unf * 1e6, 3),
+            "fused_us_per_step": round(fused_s * 1e6, 3),
+            "tflops": round(w.flops / t_unf / 1e12, 3), "speedup": round(speedup, 4),
+            "theoretical_speedup": round(theoretical, 4),
+            "fusion_efficiency": round(speedup / theoretical, 4),
+            "ai_fused": round(ai_fused, 2), "ai_unfused": round(ai_unfused, 2),
+            "ai_increase_pct": round(100 * (ai_fused / ai_unfused - 1), 2),
+            "intermediate_bytes_removed": extra}
 
 
 # ---------------------------------------------------------- oracle timing ----
@@ -423,6 +482,8 @@ def main(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--compare-unfused", action="store_true",
+                   help="also time the unfused PyTorch eager path and report the derived metrics")
     args = p.parse_args(argv)
     args.warmup = max(args.warmup, 3)
     w = workload_by_name(args.workload)
