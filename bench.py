@@ -53,7 +53,8 @@ DEFAULT_WORKLOAD = "qwen2.5-7b-decode-m16"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = ["swiglu_gated_mlp_gb300/csrc/" + f for f in
-                  ("fused_small_m.cu", "fused_large_m.cu", "ptx.cuh", "kernels.h", "swiglu_api.cu")]
+                  ("fused_small_m.cu", "fused_large_m.cu", "fused_large_m_pair.cu", "ptx.cuh", "kernels.h",
+                   "swiglu_api.cu")]
 
 
 def workload_by_name(name: str) -> Workload:

@@ -23,6 +23,7 @@ SWIGLU_ERR_NO_DEVICE = 5
 SWIGLU_VARIANT_AUTO = 0
 SWIGLU_VARIANT_LARGE_M = 1
 SWIGLU_VARIANT_SMALL_M = 2
+SWIGLU_VARIANT_LARGE_M_PAIR = 3
 
 PACK_BLOCK_N = 128
 

@@ -1,0 +1,313 @@
+// Large-M fused SwiGLU kernel on CTA pairs: Y = SiLU(A W1) * (A W2) for
+// 256-token tiles computed by two SMs with tcgen05.mma.cta_group::2.
+//
+// Same method as fused_large_m.cu (one packed weight stream, gate and up
+// columns side by side in one fp32 TMEM accumulator, SiLU * mul epilogue
+// overlapped with the next tile's MMAs; "Tile-Level Activation Overlap for
+// Efficient LLM Inference", gist.science, section "Methodology"), with the
+// operand traffic of each SM cut by a third:
+//
+//  * a cluster of two CTAs owns a 256 x 128 output tile; CTA rank r loads A
+//    rows [128 r, 128 r + 128) of the tile and packed-weight rows
+//    [128 r, 128 r + 128) of the (column block, K slice) tile, i.e. rank 0
+//    the 128 gate columns and rank 1 the 128 matching up columns;
+//  * rank 0 issues one MMA of M=256, N=256, K=16 per step over both CTAs'
+//    shared memory; each CTA's TMEM receives its 128 rows x (128 gate | 128 up)
+//    columns, so each CTA's epilogue is the single-CTA one;
+//  * per 64-deep K step each CTA pulls 32 KB (16 KB A + 16 KB W) instead of
+//    48 KB, and the ring holds 6 stages;
+//  * both CTAs' loads complete on rank 0's "full" barrier; rank 0's MMA
+//    completions arrive on both CTAs' "empty" and "accumulator full"
+//    barriers (multicast commit); both epilogues arrive on rank 0's
+//    "accumulator empty" barrier; every wait is bounded (ptx.cuh).
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace swg {
+namespace {
+
+struct PairCfg {
+  static constexpr int kBN = 128;                        // output columns per tile
+  static constexpr int kABytes = 128 * kBlockK * 2;      // 16 KB: this CTA's 128 A rows
+  static constexpr int kBBytes = 128 * kBlockK * 2;      // 16 KB: this CTA's 128 weight rows
+  static constexpr int kStageBytes = kABytes + kBBytes;  // 32 KB per CTA, 64 KB per pair
+  static constexpr int kStages = 6;
+  static constexpr int kAccCols = 2 * kBN;               // 256 fp32 columns: gate | up
+  static constexpr int kTmemCols = 2 * kAccCols;         // double buffered
+  static constexpr int kStgBytes = 32 * 32 * 2;          // 32 rows x 64 B store staging
+  static constexpr int kNumStg = 8;
+  static constexpr int kBarBytes = 256;
+  static constexpr size_t kSmem =
+      1024 + size_t(kStages) * kStageBytes + size_t(kNumStg) * kStgBytes + kBarBytes;
+  static_assert(kSmem <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ void pair_tile_coords(int t, int tiles_m, int tiles_n, int group_m,
+                                                 int& mb, int& nb) {
+  const int per_group = group_m * tiles_n;
+  const int g = t / per_group;
+  const int first_m = g * group_m;
+  const int gm = min(tiles_m - first_m, group_m);
+  const int r = t - g * per_group;
+  mb = first_m + r % gm;
+  nb = r / gm;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    fused_large_m_pair_kernel(const __grid_constant__ LargeMParams p) {
+  using C = PairCfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sA = smem_addr(smem);
+  const uint32_t sB = sA + C::kStages * C::kABytes;
+  const uint32_t sStg = sB + C::kStages * C::kBBytes;
+  uint8_t* bar_ptr = smem + size_t(C::kStages) * C::kStageBytes + C::kNumStg * C::kStgBytes;
+  const uint32_t bar0 = smem_addr(bar_ptr);
+  // barrier slots: full[S] | empty[S] | tmem_full[2] | tmem_empty[2] | drain
+  const uint32_t full0 = bar0, empty0 = bar0 + 8u * C::kStages;
+  const uint32_t tfull0 = bar0 + 16u * C::kStages, tempty0 = tfull0 + 16u;
+  const uint32_t drain_bar = tempty0 + 16u;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_ptr + 8 * (2 * C::kStages + 5));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = static_cast<int>(cluster_id_x());
+  const int pairs = static_cast<int>(cluster_count_x());
+  const int num_tiles = p.tiles_m * p.tiles_n;
+  const int num_kb = (p.K + kBlockK - 1) / kBlockK;
+  const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
+  // rank 0's full and tmem_empty barriers, as seen from either CTA of the pair
+  const uint32_t full0_lead = mapa_shared(full0, 0);
+  const uint32_t tempty0_lead = mapa_shared(tempty0, 0);
+
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&p.tmap_a);
+    prefetch_tmap(&p.tmap_w);
+    prefetch_tmap(&p.tmap_y);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(full0 + 8u * s, 1);   // rank 0's producer arrives (with both CTAs' bytes)
+      mbar_init(empty0 + 8u * s, 1);  // rank 0's MMA commit, multicast to both CTAs
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull0 + 8u * b, 1);   // multicast MMA commit
+      mbar_init(tempty0 + 8u * b, 8);  // 4 epilogue warps x 2 CTAs (used on rank 0)
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_addr(tmem_slot), C::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
+  tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  pdl_wait();
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t filled = 0, fill_ph = 0;
+      bool skip_once = p.inject_stall != 0;
+      bool ok = true;
+      for (int t = pair; ok && t < num_tiles; t += pairs) {
+        int mb, nb;
+        pair_tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, mb, nb);
+        const int m0 = mb * 2 * kTileM + static_cast<int>(rank) * kTileM;
+        const int wtile = nb * num_kb;                        // (column block nb, K slice 0)
+        const int wrow = static_cast<int>(rank) * kPackBlockN;  // gate rows (0) / up rows (1)
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(empty0 + 8u * s, ph ^ 1u, wc, kSiteProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          if (skip_once) {
+            skip_once = false;  // testing hook: both CTAs leave this stage unfilled
+          } else {
+            if (leader) mbar_arrive_expect_tx(full0 + 8u * s, 2 * C::kStageBytes);
+            const uint32_t fb = full0_lead + 8u * s;
+            tma_load_2d_pair(sA + s * C::kABytes, &p.tmap_a, fb, kb * kBlockK, m0);
+            tma_load_3d_pair(sB + s * C::kBBytes, &p.tmap_w, fb, 0, wrow, wtile + kb);
+            filled |= 1u << s;
+            fill_ph = (fill_ph & ~(1u << s)) | (ph << s);
+          }
+          if (++s == C::kStages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      pdl_launch_dependents();
+      // Rank 0's full barriers count both CTAs' bytes: once they complete, every
+      // copy issued by the pair for those stages has landed.
+      if (leader)
+        for (int i = 0; i < C::kStages; ++i)
+          if (filled & (1u << i)) mbar_wait_drain(full0 + 8u * i, (fill_ph >> i) & 1u, wc);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer (rank 0)
+    if (leader && lane == 0) {
+      constexpr uint32_t kIdesc = idesc_bf16_f32(2 * kTileM, 2 * C::kBN);
+      int s = 0;
+      uint32_t ph = 0;
+      int buf = 0;
+      uint32_t acc_ph = 0;
+      bool ok = true;
+      for (int t = pair; ok && t < num_tiles; t += pairs) {
+        if (!mbar_wait(tempty0 + 8u * buf, acc_ph ^ 1u, wc, kSiteMmaTmemEmpty)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + buf * C::kAccCols;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(full0 + 8u * s, ph, wc, kSiteMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = smem_desc_sw128(sA + s * C::kABytes);
+          const uint64_t bdesc = smem_desc_sw128(sB + s * C::kBBytes);
+#pragma unroll
+          for (int k = 0; k < kBlockK / 16; ++k)
+            mma_bf16_pair(d, adesc + 2u * k, bdesc + 2u * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
+          mma_commit_pair_multicast(empty0 + 8u * s, 0x3);  // frees the stage in both CTAs
+          if (++s == C::kStages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair_multicast(tfull0 + 8u * buf, 0x3);  // both halves of the accumulator ready
+        buf ^= 1;
+        if (buf == 0) acc_ph ^= 1u;
+      }
+      mma_commit_pair_multicast(drain_bar, 0x1);
+      mbar_wait_drain(drain_bar, 0, wc);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const int ew = warp - 2;
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    int buf = 0;
+    uint32_t acc_ph = 0;
+    int sbuf = 0;
+    for (int t = pair; t < num_tiles; t += pairs) {
+      int mb, nb;
+      pair_tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, mb, nb);
+      const int row0 = mb * 2 * kTileM + static_cast<int>(rank) * kTileM + q * 32;
+      const int col0 = nb * C::kBN;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(tfull0 + 8u * buf, acc_ph, wc, kSiteEpiTmemFull) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + lane_off + buf * C::kAccCols;
+#pragma unroll 1
+      for (int c = 0; c < C::kBN / 32; ++c) {
+        uint32_t g[32], u[32];
+        tmem_ld_x32(tacc + c * 32, g);
+        tmem_ld_x32(tacc + C::kBN + c * 32, u);
+        tmem_wait_ld();
+        reg_fence(g);
+        reg_fence(u);
+        if (c == C::kBN / 32 - 1) {  // this CTA's half of the accumulator is read
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(tempty0_lead + 8u * buf);
+        }
+        if (lane == 0) bulk_wait_read<1>();
+        __syncwarp();
+        const uint32_t stg = sStg + (ew * 2 + sbuf) * C::kStgBytes;
+        const uint32_t row_addr = stg + lane * 64;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i0 = 8 * j + 2 * e;
+            w[e] = pack_bf16x2(silu_mul(__uint_as_float(g[i0]), __uint_as_float(u[i0])),
+                               silu_mul(__uint_as_float(g[i0 + 1]), __uint_as_float(u[i0 + 1])));
+          }
+          st_shared_v4(row_addr + ((j ^ ((lane >> 1) & 3)) << 4), w[0], w[1], w[2], w[3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int ncol = col0 + c * 32;
+          if (ncol < p.N && row0 < p.M) tma_store_2d(&p.tmap_y, stg, ncol, row0);
+          bulk_commit();
+        }
+        sbuf ^= 1;
+      }
+      buf ^= 1;
+      if (buf == 0) acc_ph ^= 1u;
+    }
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
+  }
+
+  // Neither CTA leaves while the pair's MMAs may still read its shared memory
+  // or the peer may still arrive on its barriers.
+  tc_fence_before();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, C::kTmemCols);
+  }
+}
+
+cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr,
+                               bool with_pdl) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = PairCfg::kSmem;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = with_pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cfg;
+}
+
+}  // namespace
+
+cudaError_t configure_large_m_pair(int* max_pairs) {
+  cudaError_t e = cudaFuncSetAttribute(fused_large_m_pair_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(PairCfg::kSmem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = pair_config(2, nullptr, attr, false);
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, fused_large_m_pair_kernel, &cfg);
+  if (e != cudaSuccess) return e;
+  *max_pairs = clusters;
+  return cudaSuccess;
+}
+
+size_t large_m_pair_smem_bytes() { return PairCfg::kSmem; }
+int large_m_pair_stages() { return PairCfg::kStages; }
+
+cudaError_t launch_large_m_pair(const LargeMParams& p, cudaStream_t stream) {
+  if (p.grid < 2 || (p.grid % 2) != 0 || p.bn != PairCfg::kBN) return cudaErrorInvalidValue;
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = pair_config(p.grid, stream, attr, pdl_enabled());
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, fused_large_m_pair_kernel, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace swg

@@ -48,6 +48,13 @@ int large_m_stages(int bn);
 size_t large_m_smem_bytes(int bn);
 cudaError_t launch_large_m(const LargeMParams& p, cudaStream_t stream);
 
+// CTA-pair variant (bn = 128, 256-row tiles, grid = 2 x pairs): one-time set-up
+// also reports how many pairs can be resident at once.
+cudaError_t configure_large_m_pair(int* max_pairs);
+size_t large_m_pair_smem_bytes();
+int large_m_pair_stages();
+cudaError_t launch_large_m_pair(const LargeMParams& p, cudaStream_t stream);
+
 // Words of the static scratch array behind swiglu_forward_noalloc (256 bytes);
 // a call uses the first kStatusWords of them for its status record.
 constexpr int kStaticScratchWords = 64;

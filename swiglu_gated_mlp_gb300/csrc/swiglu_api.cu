@@ -22,6 +22,7 @@ struct DeviceState {
   std::atomic<bool> ready{false};
   swiglu_status_t init_status = SWIGLU_OK;
   int sm_count = 0;
+  int max_pairs = 0;           // CTA pairs of the pair kernel resident at once
   uint32_t* status = nullptr;  // uint32_t[4], see ptx.cuh
 };
 
@@ -95,6 +96,11 @@ swiglu_status_t init_device(int dev, DeviceState& d) {
     cudaGetLastError();
     return SWIGLU_ERR_CUDA;
   }
+  // The CTA-pair kernel is optional: if its set-up fails, that variant is unavailable.
+  if (swg::configure_large_m_pair(&d.max_pairs) != cudaSuccess) {
+    cudaGetLastError();
+    d.max_pairs = 0;
+  }
   return SWIGLU_OK;
 }
 
@@ -151,12 +157,19 @@ struct Plan {
   int bn = 0, stages = 0, tiles_m = 0, tiles_n = 0, group_m = 0, tiles = 0, grid = 0, mt = 0;
 };
 
-swiglu_status_t make_plan(int64_t M, int64_t K, int64_t N, int variant, int sm_count, Plan* pl) {
-  if (variant != SWIGLU_VARIANT_AUTO && variant != SWIGLU_VARIANT_LARGE_M &&
-      variant != SWIGLU_VARIANT_SMALL_M)
+swiglu_status_t make_plan(int64_t M, int64_t K, int64_t N, int variant, int sm_count,
+                          int max_pairs, Plan* pl) {
+  if (variant < SWIGLU_VARIANT_AUTO || variant > SWIGLU_VARIANT_LARGE_M_PAIR)
     return SWIGLU_ERR_INVALID_ARG;
-  if (variant == SWIGLU_VARIANT_AUTO)
+  if (variant == SWIGLU_VARIANT_AUTO) {
     variant = (M <= small_m_max() && M <= 256) ? SWIGLU_VARIANT_SMALL_M : SWIGLU_VARIANT_LARGE_M;
+    // Enough 128-row x 128-column tiles to fill the SMs: run 256-row tiles on
+    // CTA pairs (a third less operand traffic per SM).
+    if (variant == SWIGLU_VARIANT_LARGE_M && max_pairs > 0) {
+      const int64_t tiles128 = ((M + swg::kTileM - 1) / swg::kTileM) * (padded_n(N) / swg::kPackBlockN);
+      if (tiles128 >= sm_count && M > swg::kTileM) variant = SWIGLU_VARIANT_LARGE_M_PAIR;
+    }
+  }
   const int64_t np = padded_n(N);
   pl->variant = variant;
   if (variant == SWIGLU_VARIANT_SMALL_M) {
@@ -170,6 +183,23 @@ swiglu_status_t make_plan(int64_t M, int64_t K, int64_t N, int variant, int sm_c
     if (sm_count > 0 && pl->tiles > sm_count && swg::small_m_stages(pl->mt, 2) >= 3)
       pl->stages = swg::small_m_stages(pl->mt, 2);
     pl->grid = pl->tiles;
+    return SWIGLU_OK;
+  }
+  if (variant == SWIGLU_VARIANT_LARGE_M_PAIR) {
+    if (max_pairs < 1) return SWIGLU_ERR_UNSUPPORTED;
+    const int64_t pm = (M + 2 * swg::kTileM - 1) / (2 * swg::kTileM);  // 256-row tiles
+    const int64_t ptiles = pm * (np / swg::kPackBlockN);
+    if (ptiles > 2147483647) return SWIGLU_ERR_UNSUPPORTED;
+    int64_t group = (48ll << 20) / (int64_t(2 * swg::kTileM) * K * 2);
+    if (group < 1) group = 1;
+    if (group > pm) group = pm;
+    pl->bn = swg::kPackBlockN;
+    pl->stages = swg::large_m_pair_stages();
+    pl->tiles_m = static_cast<int>(pm);
+    pl->tiles_n = static_cast<int>(np / swg::kPackBlockN);
+    pl->group_m = static_cast<int>(group);
+    pl->tiles = static_cast<int>(ptiles);
+    pl->grid = 2 * static_cast<int>(ptiles < max_pairs ? ptiles : max_pairs);
     return SWIGLU_OK;
   }
   const int64_t tiles_m = (M + swg::kTileM - 1) / swg::kTileM;
@@ -258,7 +288,8 @@ swiglu_status_t launch_forward(const void* A, const void* Wp, void* Y, int64_t M
     p.status = d.status;
     p.timeout_ns = timeout;
     p.inject_stall = inject;
-    err = swg::launch_large_m(p, stream);
+    err = pl.variant == SWIGLU_VARIANT_LARGE_M_PAIR ? swg::launch_large_m_pair(p, stream)
+                                                    : swg::launch_large_m(p, stream);
   }
   if (err != cudaSuccess) {
     cudaGetLastError();
@@ -360,14 +391,14 @@ swiglu_status_t swiglu_forward_variant(const void* A, const void* Wpacked, void*
                                        swiglu_stream_t stream) {
   swiglu_status_t st = check_forward_args(A, Wpacked, Y, M, K, N);
   if (st != SWIGLU_OK) return st;
-  if (variant < SWIGLU_VARIANT_AUTO || variant > SWIGLU_VARIANT_SMALL_M)
+  if (variant < SWIGLU_VARIANT_AUTO || variant > SWIGLU_VARIANT_LARGE_M_PAIR)
     return SWIGLU_ERR_INVALID_ARG;
   if (M == 0) return SWIGLU_OK;
   DeviceState* d = nullptr;
   st = device_state(&d);
   if (st != SWIGLU_OK) return st;
   Plan pl;
-  st = make_plan(M, K, N, variant, d->sm_count, &pl);
+  st = make_plan(M, K, N, variant, d->sm_count, d->max_pairs, &pl);
   if (st != SWIGLU_OK) return st;
   return launch_forward(A, Wpacked, Y, M, K, N, pl, *d, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -394,7 +425,7 @@ swiglu_status_t swiglu_forward_from_host(const void* A_host, const void* Wpacked
     return SWIGLU_ERR_CUDA;
   }
   Plan pl;
-  st = make_plan(M, K, N, SWIGLU_VARIANT_AUTO, d->sm_count, &pl);
+  st = make_plan(M, K, N, SWIGLU_VARIANT_AUTO, d->sm_count, d->max_pairs, &pl);
   if (st != SWIGLU_OK) return st;
   st = launch_forward(A_dev, Wpacked, Y_dev, M, K, N, pl, *d, s);
   if (st != SWIGLU_OK) return st;
@@ -452,11 +483,15 @@ swiglu_status_t swiglu_plan_string(int64_t M, int64_t K, int64_t N, int variant,
   st = device_state(&d);
   if (st != SWIGLU_OK) return st;
   Plan pl;
-  st = make_plan(M < 1 ? 1 : M, K, N, variant, d->sm_count, &pl);
+  st = make_plan(M < 1 ? 1 : M, K, N, variant, d->sm_count, d->max_pairs, &pl);
   if (st != SWIGLU_OK) return st;
   if (pl.variant == SWIGLU_VARIANT_SMALL_M)
     std::snprintf(buf, buflen, "small_m mt=%d stages=%d tiles=%d grid=%d sms=%d", pl.mt,
                   pl.stages, pl.tiles, pl.grid, d->sm_count);
+  else if (pl.variant == SWIGLU_VARIANT_LARGE_M_PAIR)
+    std::snprintf(buf, buflen,
+                  "large_m_pair bn=%d stages=%d tiles=%d grid=%d group_m=%d max_pairs=%d sms=%d",
+                  pl.bn, pl.stages, pl.tiles, pl.grid, pl.group_m, d->max_pairs, d->sm_count);
   else
     std::snprintf(buf, buflen, "large_m bn=%d stages=%d tiles=%d grid=%d group_m=%d sms=%d",
                   pl.bn, pl.stages, pl.tiles, pl.grid, pl.group_m, d->sm_count);
@@ -478,7 +513,7 @@ swiglu_status_t swiglu_forward_noalloc(const void* A, const void* Wpacked, void*
   st = noalloc_state(&s);
   if (st != SWIGLU_OK) return st;
   Plan pl;
-  st = make_plan(M, K, N, SWIGLU_VARIANT_SMALL_M, 0, &pl);
+  st = make_plan(M, K, N, SWIGLU_VARIANT_SMALL_M, 0, 0, &pl);
   if (st != SWIGLU_OK) return st;
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   // The shared array keeps the previous call's record: the status must start at zero.

@@ -18,7 +18,7 @@ from gpu_helpers import (check_against_oracle, run_forward, sentinel_buffer, sen
 
 pytestmark = pytest.mark.gpu
 
-AUTO, LARGE, SMALL = 0, 1, 2
+AUTO, LARGE, SMALL, PAIR = 0, 1, 2, 3
 
 
 @pytest.fixture(scope="module")
@@ -66,12 +66,23 @@ def test_large_m_kernel_matches_oracle(native, M, K, N):
     check_against_oracle(native, M, K, N, seed=M * 5 + K + N, variant=LARGE)
 
 
+PAIR_CASES = [
+    (1, 64, 128), (100, 200, 264), (256, 64, 128), (257, 136, 256), (300, 512, 1000),
+    (1000, 256, 512), (513, 896, 4864), (512, 3584, 1024), (384, 72, 8), (2048, 128, 2048),
+]
+
+
+@pytest.mark.parametrize("M,K,N", PAIR_CASES)
+def test_pair_kernel_matches_oracle(native, M, K, N):
+    check_against_oracle(native, M, K, N, seed=M * 3 + K + N, variant=PAIR)
+
+
 @pytest.mark.parametrize("M,K,N", AUTO_CASES)
 def test_auto_choice_matches_oracle(native, M, K, N):
     check_against_oracle(native, M, K, N, seed=M + K + N, variant=AUTO)
 
 
-@pytest.mark.parametrize("variant", [LARGE, SMALL])
+@pytest.mark.parametrize("variant", [LARGE, SMALL, PAIR])
 def test_variants_agree(native, variant):
     # both kernels accumulate in fp32; their bf16 outputs agree within 1 ulp-ish
     a, w1, w2 = make_inputs(48, 640, 512, seed=77)
@@ -122,7 +133,7 @@ def test_identity_slice(native, variant):
 
 # ------------------------------------------------- memory and streams ----
 
-@pytest.mark.parametrize("variant,M", [(LARGE, 200), (SMALL, 9), (LARGE, 5)])
+@pytest.mark.parametrize("variant,M", [(LARGE, 200), (SMALL, 9), (LARGE, 5), (PAIR, 300)])
 def test_writes_stay_inside_y(native, variant, M):
     K, N, pad = 128, 392, 4096
     a, w1, w2 = make_inputs(M, K, N, seed=8)
@@ -181,4 +192,5 @@ def test_forward_from_host_buffers(native):
 
 def test_plan_string_names_a_kernel(native):
     assert native.swiglu_plan_string(16, 3584, 18944).startswith("small_m")
-    assert native.swiglu_plan_string(4096, 3584, 18944).startswith("large_m bn=128")
+    assert native.swiglu_plan_string(4096, 3584, 18944).startswith("large_m_pair bn=128")
+    assert native.swiglu_plan_string(4096, 3584, 18944, 1).startswith("large_m bn=128")
