@@ -8,7 +8,9 @@ packed weight is prepared once, before timing, as at model load). Prints one
 JSON line (rank 0). Metric: TFLOP/s counted as 4*M*K*N per step.
 
 * value: whole-job TFLOP/s with inputs resident in HBM; K steps timed with
-  CUDA events between barriers + synchronisations, max over ranks.
+  CUDA events between barriers + synchronisations, max over ranks. The steps
+  replay from CUDA graphs captured from swiglu_forward calls (--eager: one
+  host call per step).
 * roofline: the fused kernel's achieved bytes/s (decode workloads, HBM bound)
   or FLOP/s (prefill workloads, tensor bound) per launch (timed region over
   launches: one launch per step), against the measured peaks in
@@ -235,14 +237,29 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
         step(i)
     sg.swiglu_check_device_status(stream=stream)
 
+    # Steps replay from CUDA graphs (one kernel node per step, captured from the
+    # same swiglu_forward calls), so the host's per-call cost does not pace
+    # microsecond-scale launches; the e2e leg below keeps per-call launches.
+    run_steps, graph_note = eager_runner(step), "eager launches"
+    if not args.eager:
+        try:
+            run_steps = graph_runner(sg, As, wps, Ys, N, copies, stream)
+            graph_note = (f"CUDA graph replay: graphs of {run_steps.block_steps} steps "
+                          f"(turns of the {copies}-slot rotation) and single-step graphs for "
+                          f"the remainder; one kernel node per step")
+        except Exception as exc:  # capture refused: keep eager launches, say so
+            graph_note = f"eager launches (graph capture failed: {type(exc).__name__})"
+            torch.cuda.synchronize()
+    run_steps(2 * copies)
+    torch.cuda.synchronize()
+
     steps = args.steps
     if steps <= 0:  # auto: about two seconds of timed work
         t0 = time.perf_counter()
-        for i in range(20):
-            step(i)
+        run_steps(4 * copies)
         torch.cuda.synchronize()
-        est = (time.perf_counter() - t0) / 20
-        steps = int(min(max(50, 2.0 / max(est, 1e-6)), 50000))
+        est = (time.perf_counter() - t0) / (4 * copies)
+        steps = int(min(max(50, 2.0 / max(est, 1e-6)), 200000))
 
     t_begin = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
@@ -251,8 +268,7 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     torch.cuda.synchronize()
     with sampler:
         t_begin.record(stream)
-        for i in range(steps):
-            step(i)
+        run_steps(steps)
         t_end.record(stream)
         torch.cuda.synchronize()
     barrier(world)
@@ -319,6 +335,7 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
         "data": "synthetic",
         "config": {"workload": w.name, "M": M, "K": K, "N": N, "seed": w.seed,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "launch": graph_note,
                    "l2": f"inputs larger than L2: {copies} rotating copies of A, packed W and Y "
                          f"({copies * w.algorithmic_bytes / 2**20:.0f} MiB)",
                    "note": w.note},
@@ -335,6 +352,49 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
     return out
+
+
+# ------------------------------------------------------------ step runners ----
+
+def eager_runner(step):
+    def run(n):
+        for i in range(n):
+            step(i)
+    return run
+
+
+def graph_runner(sg, As, wps, Ys, N, copies, stream, min_block=64):
+    """Captures the fused forward into CUDA graphs.
+
+    One graph holds `block` consecutive steps (whole turns of the rotation, at
+    least `min_block` steps, so consecutive kernels inside it overlap their
+    launches), and single-step graphs cover a remainder.
+    """
+    block_steps = copies * max(1, -(-min_block // copies))
+    side = torch.cuda.Stream(stream.device)
+    side.wait_stream(stream)
+    block = torch.cuda.CUDAGraph()
+    singles = []
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(block, stream=side):
+            for i in range(block_steps):
+                j = i % copies
+                sg.swiglu_forward(As[j], wps[j], N, Y=Ys[j])
+        for j in range(copies):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                sg.swiglu_forward(As[j], wps[j], N, Y=Ys[j])
+            singles.append(g)
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+
+    def run(n):
+        for _ in range(n // block_steps):
+            block.replay()
+        for i in range(n % block_steps):
+            singles[i % copies].replay()
+    run.block_steps = block_steps
+    return run
 
 
 # ------------------------------------------------------ unfused comparator ----
@@ -483,6 +543,8 @@ def main(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--eager", action="store_true",
+                   help="time per-call launches instead of CUDA graph replay")
     p.add_argument("--compare-unfused", action="store_true",
                    help="also time the unfused PyTorch eager path and report the derived metrics")
     args = p.parse_args(argv)

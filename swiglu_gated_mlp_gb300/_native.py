@@ -68,10 +68,34 @@ def _check(code: int, where: str) -> None:
         raise SwigluError(code, where)
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream_handle(stream, device) -> int:
     if stream is None:
+        if _raw_stream is not None:  # the current stream's handle without a Stream object
+            return _raw_stream(device.index if device.index is not None
+                               else torch.cuda.current_device())
         stream = torch.cuda.current_stream(device)
     return int(stream.cuda_stream) if isinstance(stream, torch.cuda.Stream) else int(stream)
+
+
+class _on_device:
+    """Makes `device` current for the library call (a no-op when it already is)."""
+    __slots__ = ("idx", "prev")
+
+    def __init__(self, device):
+        self.idx = device.index if device.index is not None else torch.cuda.current_device()
+
+    def __enter__(self):
+        self.prev = torch.cuda.current_device()
+        if self.prev != self.idx:
+            torch.cuda.set_device(self.idx)
+
+    def __exit__(self, *exc):
+        if self.prev != self.idx:
+            torch.cuda.set_device(self.prev)
+        return False
 
 
 def _dev_bf16(t: torch.Tensor, name: str) -> None:
@@ -109,7 +133,7 @@ def swiglu_pack_weights(W1: torch.Tensor, W2: torch.Tensor, Wpacked: torch.Tenso
     _dev_bf16(Wpacked, "Wpacked")
     if Wpacked.numel() * 2 < swiglu_packed_weight_bytes(K, N):
         raise ValueError("Wpacked is too small")
-    with torch.cuda.device(W1.device):
+    with _on_device(W1.device):
         _check(lib.swiglu_pack_weights(W1.data_ptr(), W2.data_ptr(), Wpacked.data_ptr(), K, N,
                                        _stream_handle(stream, W1.device)), "swiglu_pack_weights")
     return Wpacked
@@ -129,7 +153,7 @@ def swiglu_forward_variant(A: torch.Tensor, Wpacked: torch.Tensor, N: int, varia
     _dev_bf16(Y, "Y")
     if tuple(Y.shape) != (M, N):
         raise ValueError("Y must be [M, N]")
-    with torch.cuda.device(A.device):
+    with _on_device(A.device):
         _check(lib.swiglu_forward_variant(A.data_ptr(), Wpacked.data_ptr(), Y.data_ptr(), M, K, N,
                                           int(variant), _stream_handle(stream, A.device)),
                "swiglu_forward")
@@ -155,7 +179,7 @@ def swiglu_forward_from_host(A_host: torch.Tensor, Wpacked: torch.Tensor, N: int
     M, K = A_host.shape
     if tuple(A_dev.shape) != (M, K) or tuple(Y_host.shape) != (M, N) or tuple(Y_dev.shape) != (M, N):
         raise ValueError("shape mismatch between host and device buffers")
-    with torch.cuda.device(A_dev.device):
+    with _on_device(A_dev.device):
         _check(lib.swiglu_forward_from_host(A_host.data_ptr(), Wpacked.data_ptr(), Y_host.data_ptr(),
                                             A_dev.data_ptr(), Y_dev.data_ptr(), M, K, N,
                                             _stream_handle(stream, A_dev.device)),
@@ -177,7 +201,7 @@ def swiglu_forward_noalloc(A: torch.Tensor, Wpacked: torch.Tensor, N: int, Y: to
     if tuple(Y.shape) != (M, N):
         raise ValueError("Y must be [M, N]")
     ptr = ctypes.addressof(status_out) if status_out is not None else None
-    with torch.cuda.device(A.device):
+    with _on_device(A.device):
         _check(lib.swiglu_forward_noalloc(A.data_ptr(), Wpacked.data_ptr(), Y.data_ptr(), M, K, N,
                                           ptr, _stream_handle(stream, A.device)),
                "swiglu_forward_noalloc")

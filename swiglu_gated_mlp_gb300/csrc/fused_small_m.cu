@@ -14,6 +14,13 @@
 // thread for weight column n reads gate and up for all tokens, applies
 // SiLU(g) * u in fp32 and writes Y[m][n] (a warp writes 32 consecutive
 // columns of one row at a time).
+//
+// When there are few column blocks for the SMs (small N), each block's K range
+// is split over a cluster of `splits` CTAs: every CTA accumulates its K part in
+// TMEM, writes the fp32 partial Gate and Up to its own shared memory, and after
+// a cluster barrier each CTA sums, through distributed shared memory, all
+// parts of its share of the block's columns, applies SiLU(g) * u and writes
+// those outputs. No global scratch is used.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -57,7 +64,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int num_kb = (p.K + kBlockK - 1) / kBlockK;
-  const int nblk = blockIdx.x;
+  const int splits = p.splits > 1 ? p.splits : 1;
+  const int nblk = blockIdx.x / splits;
+  const int part = blockIdx.x % splits;  // the CTA's rank in its cluster when splits > 1
+  const int kb_begin = part * num_kb / splits;
+  const int kb_end = (part + 1) * num_kb / splits;
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
 
   if (threadIdx.x == 0) {
@@ -92,7 +103,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0;
       uint32_t filled = 0, fill_ph = 0;
       bool skip_once = p.inject_stall != 0;
-      for (int kb = 0; kb < num_kb; ++kb) {
+      for (int kb = kb_begin; kb < kb_end; ++kb) {
         if (!mbar_wait(empty0 + 8u * s, ph ^ 1u, wc, kSiteProducerEmpty)) break;
         if (skip_once) {
           skip_once = false;  // testing hook: leave this stage unfilled
@@ -125,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int kb = 0; kb < num_kb; ++kb) {
+      for (int kb = kb_begin; kb < kb_end; ++kb) {
         if (!mbar_wait(full0 + 8u * s, ph, wc, kSiteMmaFull)) {
           ok = false;
           break;
@@ -137,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t xdesc = smem_desc_sw128(sw + kWStageBytes);          // tokens
 #pragma unroll
         for (int k = 0; k < kBlockK / 16; ++k) {
-          const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
+          const uint32_t acc = (kb != kb_begin || k != 0) ? 1u : 0u;
           mma_bf16(d_gate, gdesc + 2u * k, xdesc + 2u * k, idesc, acc);
           mma_bf16(d_up, udesc + 2u * k, xdesc + 2u * k, idesc, acc);
         }
@@ -160,7 +171,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     int ok = 1;
     if (lane == 0) ok = mbar_wait(tfull_bar, 0, wc, kSiteEpiTmemFull) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok) {
+    if (ok && splits > 1) {
+      // K part only: fp32 partials to this CTA's shared memory (the ring is idle
+      // now), as P[c][r] for accumulator column c (gate 0..mt-1, up mt..2mt-1)
+      // and weight row r of the block.
+      tc_fence_after();
+      float* part_buf = reinterpret_cast<float*>(smem);
+      const int r = q * 32 + lane;
+#pragma unroll 1
+      for (int mc = 0; mc < mt / 16; ++mc) {
+        uint32_t g[16], u[16];
+        tmem_ld_x16(tmem_base + lane_off + mc * 16, g);
+        tmem_ld_x16(tmem_base + lane_off + mt + mc * 16, u);
+        tmem_wait_ld();
+        reg_fence(g);
+        reg_fence(u);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          part_buf[(mc * 16 + j) * kPackBlockN + r] = __uint_as_float(g[j]);
+          part_buf[(mt + mc * 16 + j) * kPackBlockN + r] = __uint_as_float(u[j]);
+        }
+      }
+    } else if (ok) {
       tc_fence_after();
       __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(p.y);
 #pragma unroll 1
@@ -183,6 +215,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
+  }
+
+  if (splits > 1) {
+    cluster_sync();  // every part's partials are in its CTA's shared memory
+    // This CTA finishes weight rows [part * R, part * R + R) of the block for
+    // all tokens: sum the parts (fixed order), SiLU(g) * u, 4 columns per item.
+    const int rows = kPackBlockN / splits;
+    const int chunks = rows / 4;
+    const uint32_t local = smem_addr(smem);
+    __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(p.y);
+    for (int idx = threadIdx.x; idx < p.M * chunks; idx += blockDim.x) {
+      const int m = idx / chunks;
+      const int r = part * rows + (idx % chunks) * 4;
+      float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+      for (int s = 0; s < splits; ++s) {
+        const uint32_t base = mapa_shared(local, static_cast<uint32_t>(s));
+        const float4 gs = ld_shared_cluster_v4(base + 4u * static_cast<uint32_t>(m * kPackBlockN + r));
+        const float4 us =
+            ld_shared_cluster_v4(base + 4u * static_cast<uint32_t>((mt + m) * kPackBlockN + r));
+        g.x += gs.x; g.y += gs.y; g.z += gs.z; g.w += gs.w;
+        u.x += us.x; u.y += us.y; u.z += us.z; u.w += us.w;
+      }
+      const int n = nblk * kPackBlockN + r;  // N % 8 == 0: n < N implies n + 3 < N
+      if (n < p.N) {
+        uint2 v;
+        v.x = pack_bf16x2(silu_mul(g.x, u.x), silu_mul(g.y, u.y));
+        v.y = pack_bf16x2(silu_mul(g.z, u.z), silu_mul(g.w, u.w));
+        *reinterpret_cast<uint2*>(y + static_cast<size_t>(m) * p.N + n) = v;
+      }
+    }
+    cluster_sync();  // no CTA leaves while a peer may still read its partials
   }
 
   tc_fence_before();
@@ -228,19 +291,50 @@ cudaError_t static_scratch_address(uint32_t** out) {
   return cudaSuccess;
 }
 
+int small_m_max_clusters(int splits) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(splits);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemLimit;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = splits;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, fused_small_m_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return clusters;
+}
+
 cudaError_t launch_small_m(const SmallMParams& p, cudaStream_t stream) {
   if (p.stages < 2 || p.stages > kMaxStages || p.mt < 16 || p.mt > 256 || (p.mt % 16) != 0)
+    return cudaErrorInvalidValue;
+  const int splits = p.splits > 1 ? p.splits : 1;
+  const int num_kb = (p.K + kBlockK - 1) / kBlockK;
+  if (splits > 1 &&
+      (splits > 8 || (kPackBlockN % (4 * splits)) != 0 || splits > num_kb || p.mt > 128 ||
+       size_t(2) * p.mt * kPackBlockN * 4 > size_t(p.stages) * (kWStageBytes + size_t(p.mt) * kBlockK * 2) ||
+       (p.grid % splits) != 0))
     return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(p.grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = small_m_smem_bytes(p.mt, p.stages);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = splits;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = splits > 1 ? 2 : 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, fused_small_m_kernel, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -34,7 +34,8 @@ struct SmallMParams {
   int M, K, N;
   int mt;      // tokens rounded up to a multiple of 16 (MMA N), <= 256
   int stages;  // pipeline depth
-  int grid;    // one CTA per 128-column block
+  int grid;    // one CTA per 128-column block and K part (splits)
+  int splits;  // K parts per column block (<= 1: none); > 1: clusters of `splits` CTAs
   uint32_t* status;
   uint64_t timeout_ns;
   int inject_stall;
@@ -71,6 +72,9 @@ int small_m_stages(int mt, int ctas_per_sm);
 bool pdl_enabled();
 size_t small_m_smem_bytes(int mt, int stages);
 cudaError_t launch_small_m(const SmallMParams& p, cudaStream_t stream);
+// Clusters of `splits` decode CTAs (shared memory at the 1-CTA-per-SM limit)
+// that can be resident at once; 0 if such clusters cannot be launched.
+int small_m_max_clusters(int splits);
 
 cudaError_t launch_pack(const void* w1, const void* w2, void* wp, int K, int N,
                         cudaStream_t stream);

@@ -23,6 +23,7 @@ struct DeviceState {
   swiglu_status_t init_status = SWIGLU_OK;
   int sm_count = 0;
   int max_pairs = 0;           // CTA pairs of the pair kernel resident at once
+  int small_clusters[9] = {};  // decode-kernel clusters of s CTAs resident at once (s = 2, 4, 8)
   uint32_t* status = nullptr;  // uint32_t[4], see ptx.cuh
 };
 
@@ -42,7 +43,7 @@ int64_t env_int(const char* name, int64_t dflt) {
 
 // Largest M for which AUTO picks the small-M (weights-as-MMA-M) kernel.
 int64_t small_m_max() {
-  static const int64_t v = env_int("SWIGLU_SMALL_M_MAX", 64);
+  static const int64_t v = env_int("SWIGLU_SMALL_M_MAX", 32);
   return v;
 }
 
@@ -96,6 +97,7 @@ swiglu_status_t init_device(int dev, DeviceState& d) {
     cudaGetLastError();
     return SWIGLU_ERR_CUDA;
   }
+  for (int s : {2, 4, 8}) d.small_clusters[s] = swg::small_m_max_clusters(s);
   // The CTA-pair kernel is optional: if its set-up fails, that variant is unavailable.
   if (swg::configure_large_m_pair(&d.max_pairs) != cudaSuccess) {
     cudaGetLastError();
@@ -123,17 +125,67 @@ swiglu_status_t device_state(DeviceState** out) {
   return d.init_status;
 }
 
+// Tensor-map encoding with a small per-thread cache: a decode step calls the
+// library with the same few buffers over and over, and encoding is a fixed
+// host cost on every call. Entries are keyed on every encoded field.
+struct TmapKey {
+  const void* base;
+  cuuint64_t dims[3];
+  cuuint64_t strides[2];
+  cuuint32_t box[3];
+  int rank;
+  int swizzle;
+  bool operator==(const TmapKey& o) const { return std::memcmp(this, &o, sizeof(TmapKey)) == 0; }
+};
+
+constexpr int kTmapCacheSize = 16;
+struct TmapCache {
+  TmapKey key[kTmapCacheSize];
+  CUtensorMap map[kTmapCacheSize];
+  bool used[kTmapCacheSize] = {};
+  int next = 0;
+};
+thread_local TmapCache t_tmap_cache;
+
+bool encode_cached(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+                   const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swizzle) {
+  TmapKey k;
+  std::memset(&k, 0, sizeof(k));
+  k.base = base;
+  k.rank = rank;
+  k.swizzle = static_cast<int>(swizzle);
+  for (int i = 0; i < rank; ++i) {
+    k.dims[i] = dims[i];
+    k.box[i] = box[i];
+    if (i + 1 < rank) k.strides[i] = strides[i];
+  }
+  TmapCache& c = t_tmap_cache;
+  for (int i = 0; i < kTmapCacheSize; ++i) {
+    if (c.used[i] && c.key[i] == k) {
+      *map = c.map[i];
+      return true;
+    }
+  }
+  cuuint32_t estr[3] = {1, 1, 1};
+  if (g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base),
+               const_cast<cuuint64_t*>(dims), const_cast<cuuint64_t*>(strides),
+               const_cast<cuuint32_t*>(box), estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  c.key[c.next] = k;
+  c.map[c.next] = *map;
+  c.used[c.next] = true;
+  c.next = (c.next + 1) % kTmapCacheSize;
+  return true;
+}
+
 bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                CUtensorMapSwizzle swizzle) {
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  return encode_cached(map, base, 2, dims, strides, box, swizzle);
 }
 
 // The packed weight as a 3-D tensor {64 K values, 256 rows, tiles}: every tile
@@ -141,33 +193,37 @@ bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t oute
 // contiguous 32 KB span; boxes of {64, rows, 1} are taken from one tile.
 bool encode_packed_w(CUtensorMap* map, const void* base, int64_t K, int64_t N, uint32_t rows) {
   const int64_t tiles = (padded_n(N) / swg::kPackBlockN) * k_slices(K);
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(swg::kBlockK), 2u * swg::kPackBlockN,
-                        static_cast<cuuint64_t>(tiles)};
-  cuuint64_t strides[2] = {swg::kBlockK * 2, 2u * swg::kPackBlockN * swg::kBlockK * 2};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(swg::kBlockK), rows, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
-                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(swg::kBlockK), 2u * swg::kPackBlockN,
+                              static_cast<cuuint64_t>(tiles)};
+  const cuuint64_t strides[2] = {swg::kBlockK * 2, 2u * swg::kPackBlockN * swg::kBlockK * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(swg::kBlockK), rows, 1};
+  return encode_cached(map, base, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 struct Plan {
   int variant = SWIGLU_VARIANT_AUTO;
   int bn = 0, stages = 0, tiles_m = 0, tiles_n = 0, group_m = 0, tiles = 0, grid = 0, mt = 0;
+  int splits = 1;
 };
 
-swiglu_status_t make_plan(int64_t M, int64_t K, int64_t N, int variant, int sm_count,
-                          int max_pairs, Plan* pl) {
+// `d` may be null (allocation-free entry point): no SM count, no cluster data.
+swiglu_status_t make_plan(int64_t M, int64_t K, int64_t N, int variant, const DeviceState* d,
+                          Plan* pl) {
+  const int sm_count = d ? d->sm_count : 0;
+  const int max_pairs = d ? d->max_pairs : 0;
   if (variant < SWIGLU_VARIANT_AUTO || variant > SWIGLU_VARIANT_LARGE_M_PAIR)
     return SWIGLU_ERR_INVALID_ARG;
   if (variant == SWIGLU_VARIANT_AUTO) {
-    variant = (M <= small_m_max() && M <= 256) ? SWIGLU_VARIANT_SMALL_M : SWIGLU_VARIANT_LARGE_M;
-    // Enough 128-row x 128-column tiles to fill the SMs: run 256-row tiles on
-    // CTA pairs (a third less operand traffic per SM).
-    if (variant == SWIGLU_VARIANT_LARGE_M && max_pairs > 0) {
-      const int64_t tiles128 = ((M + swg::kTileM - 1) / swg::kTileM) * (padded_n(N) / swg::kPackBlockN);
-      if (tiles128 >= sm_count && M > swg::kTileM) variant = SWIGLU_VARIANT_LARGE_M_PAIR;
+    const int64_t nb = padded_n(N) / swg::kPackBlockN;
+    const int64_t tiles128 = ((M + swg::kTileM - 1) / swg::kTileM) * nb;
+    if (M <= small_m_max() && M <= 256) {
+      variant = SWIGLU_VARIANT_SMALL_M;                  // decode: stream the weights once
+    } else if (M <= 64 && sm_count > 0 && nb * 2 <= sm_count) {
+      variant = SWIGLU_VARIANT_SMALL_M;                  // few column blocks: split K in clusters
+    } else if (max_pairs > 0 && (M <= swg::kTileM ? nb > sm_count : tiles128 >= sm_count)) {
+      variant = SWIGLU_VARIANT_LARGE_M_PAIR;             // 256-row tiles on CTA pairs
+    } else {
+      variant = SWIGLU_VARIANT_LARGE_M;
     }
   }
   const int64_t np = padded_n(N);
@@ -182,7 +238,20 @@ swiglu_status_t make_plan(int64_t M, int64_t K, int64_t N, int variant, int sm_c
     pl->stages = swg::small_m_stages(pl->mt, 1);
     if (sm_count > 0 && pl->tiles > sm_count && swg::small_m_stages(pl->mt, 2) >= 3)
       pl->stages = swg::small_m_stages(pl->mt, 2);
-    pl->grid = pl->tiles;
+    // Few column blocks for the SMs: split each block's K range over a cluster
+    // of CTAs (largest split that keeps every cluster resident at once).
+    pl->splits = 1;
+    const int64_t stage_bytes = 2 * swg::kPackBlockN * swg::kBlockK * 2 + int64_t(pl->mt) * swg::kBlockK * 2;
+    // (only for few tokens: with more, the partials' exchange costs more than it saves)
+    if (d && pl->mt <= 64 && int64_t(pl->mt) * 1024 <= pl->stages * stage_bytes) {
+      for (int s : {8, 4, 2}) {
+        if (pl->tiles * s <= sm_count && s <= k_slices(K) && d->small_clusters[s] >= pl->tiles) {
+          pl->splits = s;
+          break;
+        }
+      }
+    }
+    pl->grid = pl->tiles * pl->splits;
     return SWIGLU_OK;
   }
   if (variant == SWIGLU_VARIANT_LARGE_M_PAIR) {
@@ -266,6 +335,7 @@ swiglu_status_t launch_forward(const void* A, const void* Wp, void* Y, int64_t M
     p.mt = pl.mt;
     p.stages = pl.stages;
     p.grid = pl.grid;
+    p.splits = pl.splits;
     p.status = d.status;
     p.timeout_ns = timeout;
     p.inject_stall = inject;
@@ -398,7 +468,7 @@ swiglu_status_t swiglu_forward_variant(const void* A, const void* Wpacked, void*
   st = device_state(&d);
   if (st != SWIGLU_OK) return st;
   Plan pl;
-  st = make_plan(M, K, N, variant, d->sm_count, d->max_pairs, &pl);
+  st = make_plan(M, K, N, variant, d, &pl);
   if (st != SWIGLU_OK) return st;
   return launch_forward(A, Wpacked, Y, M, K, N, pl, *d, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -425,7 +495,7 @@ swiglu_status_t swiglu_forward_from_host(const void* A_host, const void* Wpacked
     return SWIGLU_ERR_CUDA;
   }
   Plan pl;
-  st = make_plan(M, K, N, SWIGLU_VARIANT_AUTO, d->sm_count, d->max_pairs, &pl);
+  st = make_plan(M, K, N, SWIGLU_VARIANT_AUTO, d, &pl);
   if (st != SWIGLU_OK) return st;
   st = launch_forward(A_dev, Wpacked, Y_dev, M, K, N, pl, *d, s);
   if (st != SWIGLU_OK) return st;
@@ -483,11 +553,11 @@ swiglu_status_t swiglu_plan_string(int64_t M, int64_t K, int64_t N, int variant,
   st = device_state(&d);
   if (st != SWIGLU_OK) return st;
   Plan pl;
-  st = make_plan(M < 1 ? 1 : M, K, N, variant, d->sm_count, d->max_pairs, &pl);
+  st = make_plan(M < 1 ? 1 : M, K, N, variant, d, &pl);
   if (st != SWIGLU_OK) return st;
   if (pl.variant == SWIGLU_VARIANT_SMALL_M)
-    std::snprintf(buf, buflen, "small_m mt=%d stages=%d tiles=%d grid=%d sms=%d", pl.mt,
-                  pl.stages, pl.tiles, pl.grid, d->sm_count);
+    std::snprintf(buf, buflen, "small_m mt=%d stages=%d tiles=%d splits=%d grid=%d sms=%d", pl.mt,
+                  pl.stages, pl.tiles, pl.splits, pl.grid, d->sm_count);
   else if (pl.variant == SWIGLU_VARIANT_LARGE_M_PAIR)
     std::snprintf(buf, buflen,
                   "large_m_pair bn=%d stages=%d tiles=%d grid=%d group_m=%d max_pairs=%d sms=%d",
@@ -513,7 +583,7 @@ swiglu_status_t swiglu_forward_noalloc(const void* A, const void* Wpacked, void*
   st = noalloc_state(&s);
   if (st != SWIGLU_OK) return st;
   Plan pl;
-  st = make_plan(M, K, N, SWIGLU_VARIANT_SMALL_M, 0, 0, &pl);
+  st = make_plan(M, K, N, SWIGLU_VARIANT_SMALL_M, nullptr, &pl);
   if (st != SWIGLU_OK) return st;
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   // The shared array keeps the previous call's record: the status must start at zero.

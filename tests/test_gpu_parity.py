@@ -56,6 +56,21 @@ LARGE_CASES = [
 AUTO_CASES = [(16, 3584, 1280), (64, 512, 768), (65, 512, 768), (128, 896, 4864), (1024, 1024, 1024)]
 
 
+# Few column blocks: the decode kernel splits K over clusters of 2, 4 or 8 CTAs
+# and reduces the partial accumulators through distributed shared memory.
+SPLIT_CASES = [
+    (1, 896, 4864), (64, 896, 4864), (48, 896, 4864), (16, 128, 1024), (64, 136, 392),
+    (33, 520, 8), (7, 4096, 640), (60, 200, 264),
+]
+
+
+@pytest.mark.parametrize("M,K,N", SPLIT_CASES)
+def test_small_m_split_k_matches_oracle(native, M, K, N):
+    plan = native.swiglu_plan_string(M, K, N, SMALL)
+    assert "splits=1 " not in plan, plan
+    check_against_oracle(native, M, K, N, seed=M * 11 + K + N, variant=SMALL)
+
+
 @pytest.mark.parametrize("M,K,N", SMALL_CASES)
 def test_small_m_kernel_matches_oracle(native, M, K, N):
     check_against_oracle(native, M, K, N, seed=M * 7 + K + N, variant=SMALL)
