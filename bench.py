@@ -283,7 +283,9 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
 
     peaks, peak_src = load_peaks()
     hbm_bound = w.flops / w.algorithmic_bytes < peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    kernel = "fused_small_m_kernel" if plan.startswith("small_m") else "fused_large_m_kernel"
+    kernel = ("fused_small_m_kernel" if plan.startswith("small_m") else
+              "fused_large_m_pair_kernel" if plan.startswith("large_m_pair") else
+              "fused_large_m_kernel")
     traffic, traffic_src = profiled_traffic(kernel, w.name)
     if hbm_bound:
         achieved = w.algorithmic_bytes / avg_launch / 1e9

@@ -79,6 +79,12 @@ def test_forward_rejects_null_misaligned_and_aliased(native_lib):
     assert lib.swiglu_forward_variant(FAKE, FAKE * 64, FAKE * 128, 4, 64, 64, 7, None) == 1
 
 
+def test_forward_variant_rejects_unknown_variant(native_lib):
+    lib = native_lib.lib
+    for bad in (-1, 4, 99):
+        assert lib.swiglu_forward_variant(FAKE, FAKE * 64, FAKE * 256, 4, 64, 64, bad, None) == 1
+
+
 def test_forward_m_zero_is_a_no_op(native_lib):
     assert native_lib.lib.swiglu_forward(None, None, None, 0, 64, 64, None) == 0
 

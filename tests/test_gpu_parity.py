@@ -106,6 +106,23 @@ def test_variants_agree(native, variant):
     assert torch.allclose(y_auto.float(), y_var.float(), rtol=1e-2, atol=1e-3)
 
 
+# ------------------------------------------------------------ extremes ----
+
+# Long K (hundreds of pipeline phases per tile), wide N with short K (many
+# column blocks, persistent tile loops), and a tall M (many tiles per CTA).
+EXTREME_CASES = [
+    (16, 32768, 384, SMALL), (300, 32768, 256, LARGE), (512, 16384, 256, PAIR),
+    (16, 64, 131072, SMALL), (200, 64, 65536, AUTO), (20000, 128, 256, AUTO),
+]
+
+
+@pytest.mark.parametrize("M,K,N,variant", EXTREME_CASES)
+def test_extreme_shapes_match_oracle(native, M, K, N, variant):
+    from swiglu_gated_mlp_gb300.workloads import sample_rows
+    rows = sample_rows(M, 128, seed=M + K + N)
+    check_against_oracle(native, M, K, N, seed=M + 2 * K + N, variant=variant, rows=rows)
+
+
 # ------------------------------------------------------- special values ----
 
 @pytest.mark.parametrize("variant", [LARGE, SMALL])
