@@ -52,10 +52,13 @@ from swiglu_gated_mlp_gb300.workloads import (WORKLOADS, Workload, bf16_bits,  #
 
 METRIC = "fused SwiGLU-GEMM TFLOP/s (4·M·K·N) and % of GB300 dense BF16 peak"
 DEFAULT_WORKLOAD = "qwen2.5-7b-decode-m16"
+# swiglu_forward_variant's kernel choice (auto = what swiglu_forward does)
+VARIANTS = {"auto": 0, "large": 1, "small": 2, "pair": 3, "sequential": 4}
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = ["swiglu_gated_mlp_gb300/csrc/" + f for f in
-                  ("fused_small_m.cu", "fused_large_m.cu", "fused_large_m_pair.cu", "ptx.cuh", "kernels.h",
+                  ("fused_small_m.cu", "fused_large_m.cu", "fused_large_m_pair.cu", "fused_sequential.cu",
+                   "ptx.cuh", "kernels.h",
                    "swiglu_api.cu")]
 
 
@@ -226,12 +229,13 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     a0 = a_cpu.to(dev)
     As = [a0] + [a0.clone() for _ in range(copies - 1)]
     Ys = [torch.empty(M, N, dtype=torch.bfloat16, device=dev) for _ in range(copies)]
-    plan = sg.swiglu_plan_string(M, K, N)
+    variant = VARIANTS[args.variant]
+    plan = sg.swiglu_plan_string(M, K, N, variant)
     stream = torch.cuda.current_stream(dev)
 
     def step(i):
         j = i % copies
-        sg.swiglu_forward(As[j], wps[j], N, Y=Ys[j], stream=stream)
+        sg.swiglu_forward_variant(As[j], wps[j], N, variant, Y=Ys[j], stream=stream)
 
     for i in range(args.warmup):
         step(i)
@@ -243,7 +247,7 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     run_steps, graph_note = eager_runner(step), "eager launches"
     if not args.eager:
         try:
-            run_steps = graph_runner(sg, As, wps, Ys, N, copies, stream)
+            run_steps = graph_runner(sg, As, wps, Ys, N, copies, stream, variant)
             graph_note = (f"CUDA graph replay: graphs of {run_steps.block_steps} steps "
                           f"(turns of the {copies}-slot rotation) and single-step graphs for "
                           f"the remainder; one kernel node per step")
@@ -285,6 +289,7 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     hbm_bound = w.flops / w.algorithmic_bytes < peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     kernel = ("fused_small_m_kernel" if plan.startswith("small_m") else
               "fused_large_m_pair_kernel" if plan.startswith("large_m_pair") else
+              "fused_sequential_kernel" if plan.startswith("sequential") else
               "fused_large_m_kernel")
     traffic, traffic_src = profiled_traffic(kernel, w.name)
     if hbm_bound:
@@ -336,6 +341,7 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": w.name, "M": M, "K": K, "N": N, "seed": w.seed,
+                   "variant": args.variant,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "launch": graph_note,
                    "l2": f"inputs larger than L2: {copies} rotating copies of A, packed W and Y "
@@ -365,7 +371,7 @@ def eager_runner(step):
     return run
 
 
-def graph_runner(sg, As, wps, Ys, N, copies, stream, min_block=64):
+def graph_runner(sg, As, wps, Ys, N, copies, stream, variant=0, min_block=64):
     """Captures the fused forward into CUDA graphs.
 
     One graph holds `block` consecutive steps (whole turns of the rotation, at
@@ -381,11 +387,11 @@ def graph_runner(sg, As, wps, Ys, N, copies, stream, min_block=64):
         with torch.cuda.graph(block, stream=side):
             for i in range(block_steps):
                 j = i % copies
-                sg.swiglu_forward(As[j], wps[j], N, Y=Ys[j])
+                sg.swiglu_forward_variant(As[j], wps[j], N, variant, Y=Ys[j])
         for j in range(copies):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=side):
-                sg.swiglu_forward(As[j], wps[j], N, Y=Ys[j])
+                sg.swiglu_forward_variant(As[j], wps[j], N, variant, Y=Ys[j])
             singles.append(g)
     stream.wait_stream(side)
     torch.cuda.synchronize()
@@ -545,6 +551,8 @@ def main(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--variant", choices=sorted(VARIANTS), default="auto",
+                   help="kernel to time (default: the automatic choice)")
     p.add_argument("--eager", action="store_true",
                    help="time per-call launches instead of CUDA graph replay")
     p.add_argument("--compare-unfused", action="store_true",

@@ -67,7 +67,9 @@ typedef enum {
   SWIGLU_VARIANT_AUTO = 0,    /* chosen from M (and the GPU's SM count) */
   SWIGLU_VARIANT_LARGE_M = 1, /* 128-token tiles of A, weight columns as the MMA N side */
   SWIGLU_VARIANT_SMALL_M = 2, /* weights as the MMA M side, tokens as N (M <= 256) */
-  SWIGLU_VARIANT_LARGE_M_PAIR = 3 /* 256-token tiles on CTA pairs (tcgen05 cta_group::2) */
+  SWIGLU_VARIANT_LARGE_M_PAIR = 3, /* 256-token tiles on CTA pairs (tcgen05 cta_group::2) */
+  SWIGLU_VARIANT_SEQUENTIAL = 4    /* gate K loop, then up K loop with SiLU(gate) computed
+                                      meanwhile: the pages' Kernel-1 schedule, for comparison */
 } swiglu_variant_t;
 
 /*

@@ -24,6 +24,7 @@ SWIGLU_VARIANT_AUTO = 0
 SWIGLU_VARIANT_LARGE_M = 1
 SWIGLU_VARIANT_SMALL_M = 2
 SWIGLU_VARIANT_LARGE_M_PAIR = 3
+SWIGLU_VARIANT_SEQUENTIAL = 4
 
 PACK_BLOCK_N = 128
 

@@ -56,6 +56,11 @@ size_t large_m_pair_smem_bytes();
 int large_m_pair_stages();
 cudaError_t launch_large_m_pair(const LargeMParams& p, cudaStream_t stream);
 
+// Sequential gate-then-up schedule (bn = 128, 128-row tiles), an ablation.
+cudaError_t configure_sequential();
+int sequential_stages();
+cudaError_t launch_sequential(const LargeMParams& p, cudaStream_t stream);
+
 // Words of the static scratch array behind swiglu_forward_noalloc (256 bytes);
 // a call uses the first kStatusWords of them for its status record.
 constexpr int kStaticScratchWords = 64;

@@ -93,7 +93,8 @@ swiglu_status_t init_device(int dev, DeviceState& d) {
   }
   if (cudaMalloc(&d.status, 4 * sizeof(uint32_t)) != cudaSuccess ||
       cudaMemset(d.status, 0, 4 * sizeof(uint32_t)) != cudaSuccess ||
-      swg::configure_large_m() != cudaSuccess || swg::configure_small_m() != cudaSuccess) {
+      swg::configure_large_m() != cudaSuccess || swg::configure_small_m() != cudaSuccess ||
+      swg::configure_sequential() != cudaSuccess) {
     cudaGetLastError();
     return SWIGLU_ERR_CUDA;
   }
@@ -211,7 +212,7 @@ swiglu_status_t make_plan(int64_t M, int64_t K, int64_t N, int variant, const De
                           Plan* pl) {
   const int sm_count = d ? d->sm_count : 0;
   const int max_pairs = d ? d->max_pairs : 0;
-  if (variant < SWIGLU_VARIANT_AUTO || variant > SWIGLU_VARIANT_LARGE_M_PAIR)
+  if (variant < SWIGLU_VARIANT_AUTO || variant > SWIGLU_VARIANT_SEQUENTIAL)
     return SWIGLU_ERR_INVALID_ARG;
   if (variant == SWIGLU_VARIANT_AUTO) {
     const int64_t nb = padded_n(N) / swg::kPackBlockN;
@@ -252,6 +253,23 @@ swiglu_status_t make_plan(int64_t M, int64_t K, int64_t N, int variant, const De
       }
     }
     pl->grid = pl->tiles * pl->splits;
+    return SWIGLU_OK;
+  }
+  if (variant == SWIGLU_VARIANT_SEQUENTIAL) {
+    const int64_t tm = (M + swg::kTileM - 1) / swg::kTileM;
+    const int64_t tiles = tm * (np / swg::kPackBlockN);
+    if (tiles > 2147483647) return SWIGLU_ERR_UNSUPPORTED;
+    int64_t group = (48ll << 20) / (int64_t(swg::kTileM) * K * 2);
+    if (group < 1) group = 1;
+    if (group > tm) group = tm;
+    const int sms = sm_count > 0 ? sm_count : 1;
+    pl->bn = swg::kPackBlockN;
+    pl->stages = swg::sequential_stages();
+    pl->tiles_m = static_cast<int>(tm);
+    pl->tiles_n = static_cast<int>(np / swg::kPackBlockN);
+    pl->group_m = static_cast<int>(group);
+    pl->tiles = static_cast<int>(tiles);
+    pl->grid = static_cast<int>(tiles < sms ? tiles : sms);
     return SWIGLU_OK;
   }
   if (variant == SWIGLU_VARIANT_LARGE_M_PAIR) {
@@ -359,6 +377,7 @@ swiglu_status_t launch_forward(const void* A, const void* Wp, void* Y, int64_t M
     p.timeout_ns = timeout;
     p.inject_stall = inject;
     err = pl.variant == SWIGLU_VARIANT_LARGE_M_PAIR ? swg::launch_large_m_pair(p, stream)
+          : pl.variant == SWIGLU_VARIANT_SEQUENTIAL ? swg::launch_sequential(p, stream)
                                                     : swg::launch_large_m(p, stream);
   }
   if (err != cudaSuccess) {
@@ -461,7 +480,7 @@ swiglu_status_t swiglu_forward_variant(const void* A, const void* Wpacked, void*
                                        swiglu_stream_t stream) {
   swiglu_status_t st = check_forward_args(A, Wpacked, Y, M, K, N);
   if (st != SWIGLU_OK) return st;
-  if (variant < SWIGLU_VARIANT_AUTO || variant > SWIGLU_VARIANT_LARGE_M_PAIR)
+  if (variant < SWIGLU_VARIANT_AUTO || variant > SWIGLU_VARIANT_SEQUENTIAL)
     return SWIGLU_ERR_INVALID_ARG;
   if (M == 0) return SWIGLU_OK;
   DeviceState* d = nullptr;
@@ -558,6 +577,9 @@ swiglu_status_t swiglu_plan_string(int64_t M, int64_t K, int64_t N, int variant,
   if (pl.variant == SWIGLU_VARIANT_SMALL_M)
     std::snprintf(buf, buflen, "small_m mt=%d stages=%d tiles=%d splits=%d grid=%d sms=%d", pl.mt,
                   pl.stages, pl.tiles, pl.splits, pl.grid, d->sm_count);
+  else if (pl.variant == SWIGLU_VARIANT_SEQUENTIAL)
+    std::snprintf(buf, buflen, "sequential bn=%d stages=%d tiles=%d grid=%d group_m=%d sms=%d",
+                  pl.bn, pl.stages, pl.tiles, pl.grid, pl.group_m, d->sm_count);
   else if (pl.variant == SWIGLU_VARIANT_LARGE_M_PAIR)
     std::snprintf(buf, buflen,
                   "large_m_pair bn=%d stages=%d tiles=%d grid=%d group_m=%d max_pairs=%d sms=%d",

@@ -18,7 +18,7 @@ from gpu_helpers import (check_against_oracle, run_forward, sentinel_buffer, sen
 
 pytestmark = pytest.mark.gpu
 
-AUTO, LARGE, SMALL, PAIR = 0, 1, 2, 3
+AUTO, LARGE, SMALL, PAIR, SEQ = 0, 1, 2, 3, 4
 
 
 @pytest.fixture(scope="module")
@@ -92,12 +92,22 @@ def test_pair_kernel_matches_oracle(native, M, K, N):
     check_against_oracle(native, M, K, N, seed=M * 3 + K + N, variant=PAIR)
 
 
+# The pages' Kernel-1 schedule (gate K loop, then up K loop), kept for comparison.
+SEQ_CASES = [(1, 64, 128), (100, 200, 264), (129, 136, 256), (300, 512, 1000), (513, 896, 4864),
+             (2048, 128, 2048)]
+
+
+@pytest.mark.parametrize("M,K,N", SEQ_CASES)
+def test_sequential_kernel_matches_oracle(native, M, K, N):
+    check_against_oracle(native, M, K, N, seed=M * 13 + K + N, variant=SEQ)
+
+
 @pytest.mark.parametrize("M,K,N", AUTO_CASES)
 def test_auto_choice_matches_oracle(native, M, K, N):
     check_against_oracle(native, M, K, N, seed=M + K + N, variant=AUTO)
 
 
-@pytest.mark.parametrize("variant", [LARGE, SMALL, PAIR])
+@pytest.mark.parametrize("variant", [LARGE, SMALL, PAIR, SEQ])
 def test_variants_agree(native, variant):
     # both kernels accumulate in fp32; their bf16 outputs agree within 1 ulp-ish
     a, w1, w2 = make_inputs(48, 640, 512, seed=77)
@@ -165,7 +175,7 @@ def test_identity_slice(native, variant):
 
 # ------------------------------------------------- memory and streams ----
 
-@pytest.mark.parametrize("variant,M", [(LARGE, 200), (SMALL, 9), (LARGE, 5), (PAIR, 300)])
+@pytest.mark.parametrize("variant,M", [(LARGE, 200), (SMALL, 9), (LARGE, 5), (PAIR, 300), (SEQ, 150)])
 def test_writes_stay_inside_y(native, variant, M):
     K, N, pad = 128, 392, 4096
     a, w1, w2 = make_inputs(M, K, N, seed=8)
