@@ -48,7 +48,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from swiglu_gated_mlp_gb300.workloads import (WORKLOADS, Workload, bf16_bits,  # noqa: E402
-                                              make_workload_inputs, sweep_32b)
+                                              make_inputs_fp8, make_workload_inputs, sweep_32b)
 
 METRIC = "fused SwiGLU-GEMM TFLOP/s (4·M·K·N) and % of GB300 dense BF16 peak"
 DEFAULT_WORKLOAD = "qwen2.5-7b-decode-m16"
@@ -217,25 +217,39 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     dev = torch.device("cuda", torch.cuda.current_device())
     M, K, N = w.M, w.K, w.N
 
-    a_cpu, w1_cpu, w2_cpu = make_workload_inputs(w)
-    wp0 = sg.swiglu_pack_weights(w1_cpu.to(dev), w2_cpu.to(dev))
+    fp8 = args.dtype == "fp8"
+    elem = 1 if fp8 else 2
+    alg_bytes = elem * M * K + 2 * elem * K * N + 2 * M * N  # A, W1 and W2 once, Y (bf16)
+    if fp8:
+        a_cpu, w1_cpu, w2_cpu, (s_a, s_1, s_2) = make_inputs_fp8(M, K, N, w.seed)
+        wp0 = sg.swiglu_pack_weights_fp8(w1_cpu.to(dev), w2_cpu.to(dev))
+    else:
+        a_cpu, w1_cpu, w2_cpu = make_workload_inputs(w)
+        wp0 = sg.swiglu_pack_weights(w1_cpu.to(dev), w2_cpu.to(dev))
     torch.cuda.synchronize()
-    w_bytes = wp0.numel() * 2
+    w_bytes = wp0.numel() * wp0.element_size()
     # Inputs larger than L2 between consecutive steps: rotate copies of the
     # packed weight (and of A and Y) so no step finds its operands in L2.
-    copies = max(2, math.ceil(3 * L2_BYTES / max(w.algorithmic_bytes, 1)))
+    copies = max(2, math.ceil(3 * L2_BYTES / max(alg_bytes, 1)))
     copies = min(copies, 64)
     wps = [wp0] + [wp0.clone() for _ in range(copies - 1)]
     a0 = a_cpu.to(dev)
     As = [a0] + [a0.clone() for _ in range(copies - 1)]
     Ys = [torch.empty(M, N, dtype=torch.bfloat16, device=dev) for _ in range(copies)]
     variant = VARIANTS[args.variant]
-    plan = sg.swiglu_plan_string(M, K, N, variant)
+    plan = sg.swiglu_plan_string(M, K, N, variant) if not fp8 else (
+        "fp8 " + ("small_m" if M <= 64 else "large_m_pair"))
     stream = torch.cuda.current_stream(dev)
 
+    def fwd(j, s=None):
+        """One forward on rotation slot j (on stream s, default the current stream)."""
+        if fp8:
+            sg.swiglu_forward_fp8(As[j], wps[j], N, s_a, s_1, s_2, Y=Ys[j], stream=s)
+        else:
+            sg.swiglu_forward_variant(As[j], wps[j], N, variant, Y=Ys[j], stream=s)
+
     def step(i):
-        j = i % copies
-        sg.swiglu_forward_variant(As[j], wps[j], N, variant, Y=Ys[j], stream=stream)
+        fwd(i % copies, stream)
 
     for i in range(args.warmup):
         step(i)
@@ -247,7 +261,7 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     run_steps, graph_note = eager_runner(step), "eager launches"
     if not args.eager:
         try:
-            run_steps = graph_runner(sg, As, wps, Ys, N, copies, stream, variant)
+            run_steps = graph_runner(fwd, copies, stream)
             graph_note = (f"CUDA graph replay: graphs of {run_steps.block_steps} steps "
                           f"(turns of the {copies}-slot rotation) and single-step graphs for "
                           f"the remainder; one kernel node per step")
@@ -286,39 +300,54 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     avg_launch = elapsed / steps
 
     peaks, peak_src = load_peaks()
-    hbm_bound = w.flops / w.algorithmic_bytes < peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    # FP8 tensor peak: the measured bf16 figures times the nominal fp8/bf16
+    # ratio (4.5 / 2.25 PFLOP/s dense).
+    tensor_peak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
+    tensor_sus = peaks.get("bf16_tflops_sustained")
+    tensor_sus = tensor_sus * (2.0 if fp8 else 1.0) if tensor_sus else None
+    hbm_bound = w.flops / alg_bytes < tensor_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
     kernel = ("fused_small_m_kernel" if plan.startswith("small_m") else
               "fused_large_m_pair_kernel" if plan.startswith("large_m_pair") else
               "fused_sequential_kernel" if plan.startswith("sequential") else
               "fused_large_m_kernel")
     traffic, traffic_src = profiled_traffic(kernel, w.name)
+    if fp8:
+        traffic, traffic_src = None, None  # the committed ncu summaries cover the bf16 kernels
     if hbm_bound:
-        achieved = w.algorithmic_bytes / avg_launch / 1e9
+        achieved = alg_bytes / avg_launch / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": traffic, "algorithmic_bytes": w.algorithmic_bytes}
+                "traffic": traffic, "algorithmic_bytes": alg_bytes}
     else:
         achieved = w.flops / avg_launch / 1e12
-        sus = peaks.get("bf16_tflops_sustained")
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+        sus = tensor_sus
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(tensor_peak, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / tensor_peak, 4),
                 "traffic": traffic, "algorithmic_flops": w.flops,
-                "peak_sustained": sus, "frac_sustained": round(achieved / sus, 4) if sus else None}
+                "peak_sustained": round(sus, 1) if sus else None,
+                "frac_sustained": round(achieved / sus, 4) if sus else None}
     roof.update({"kernel": kernel, "plan": plan, "avg_launch_us": round(avg_launch * 1e6, 3),
-                 "peak_source": peak_src + (", burst" if not hbm_bound else ", copy bandwidth"),
+                 "peak_source": peak_src + (
+                     ", copy bandwidth" if hbm_bound else
+                     ", bf16 burst x 2 (nominal fp8/bf16 ratio)" if fp8 else ", burst"),
                  "traffic_source": traffic_src})
 
     # ---- end to end through the public API: host activations in, host output out
     a_host = [a_cpu.pin_memory()] + [a_cpu.clone().pin_memory() for _ in range(min(copies, 4) - 1)]
     y_host = [torch.empty(M, N, dtype=torch.bfloat16).pin_memory() for _ in range(len(a_host))]
-    a_dev = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+    a_dev = torch.empty(M, K, dtype=a_cpu.dtype, device=dev)
     y_dev = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
     e2e_steps = steps
 
     def e2e_step(i):
         j = i % len(a_host)
-        sg.swiglu_forward_from_host(a_host[j], wps[i % copies], N, y_host[j], a_dev, y_dev,
-                                    stream=stream)
+        if fp8:  # host copies through torch around the FP8 call
+            a_dev.copy_(a_host[j], non_blocking=True)
+            sg.swiglu_forward_fp8(a_dev, wps[i % copies], N, s_a, s_1, s_2, Y=y_dev, stream=stream)
+            y_host[j].copy_(y_dev, non_blocking=True)
+        else:
+            sg.swiglu_forward_from_host(a_host[j], wps[i % copies], N, y_host[j], a_dev, y_dev,
+                                        stream=stream)
 
     for i in range(max(3, args.warmup // 10)):
         e2e_step(i)
@@ -338,23 +367,25 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     out = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(elapsed_max / steps * 1e3, 6),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8-e4m3 (fp32 accumulate, bf16 out)" if fp8 else "bf16",
         "data": "synthetic",
         "config": {"workload": w.name, "M": M, "K": K, "N": N, "seed": w.seed,
-                   "variant": args.variant,
+                   "variant": args.variant, "inputs": args.dtype,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "launch": graph_note,
                    "l2": f"inputs larger than L2: {copies} rotating copies of A, packed W and Y "
-                         f"({copies * w.algorithmic_bytes / 2**20:.0f} MiB)",
+                         f"({copies * alg_bytes / 2**20:.0f} MiB)",
                    "note": w.note},
         "pct_bf16_peak": round(100 * value / world / peaks["bf16_tflops"], 3),
+        "pct_of_dtype_peak": round(100 * value / world / tensor_peak, 3),
         "roofline": roof,
         "e2e": e2e,
         "gpu_launches": steps,
         "clocks": sampler.summary(),
         "packed_weight_bytes": w_bytes,
     }
-    if args.compare_unfused:
+    if args.compare_unfused and not fp8:
         out["unfused"] = unfused_comparison(w, As, w1_cpu.to(dev), w2_cpu.to(dev), copies, steps,
                                             elapsed / steps, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -371,7 +402,7 @@ def eager_runner(step):
     return run
 
 
-def graph_runner(sg, As, wps, Ys, N, copies, stream, variant=0, min_block=64):
+def graph_runner(fwd, copies, stream, min_block=64):
     """Captures the fused forward into CUDA graphs.
 
     One graph holds `block` consecutive steps (whole turns of the rotation, at
@@ -386,12 +417,11 @@ def graph_runner(sg, As, wps, Ys, N, copies, stream, variant=0, min_block=64):
     with torch.cuda.stream(side):
         with torch.cuda.graph(block, stream=side):
             for i in range(block_steps):
-                j = i % copies
-                sg.swiglu_forward_variant(As[j], wps[j], N, variant, Y=Ys[j])
+                fwd(i % copies)
         for j in range(copies):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=side):
-                sg.swiglu_forward_variant(As[j], wps[j], N, variant, Y=Ys[j])
+                fwd(j)
             singles.append(g)
     stream.wait_stream(side)
     torch.cuda.synchronize()
@@ -551,6 +581,8 @@ def main(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--dtype", choices=["bf16", "fp8"], default="bf16",
+                   help="input type: bf16 (the metric's), or E4M3 with per-tensor scales")
     p.add_argument("--variant", choices=sorted(VARIANTS), default="auto",
                    help="kernel to time (default: the automatic choice)")
     p.add_argument("--eager", action="store_true",

@@ -167,6 +167,33 @@ SWIGLU_API swiglu_status_t swiglu_plan_string(int64_t M, int64_t K, int64_t N, i
                                               char* buf, size_t buflen);
 
 /*
+ * FP8 (E4M3) form of the op. The pages point out that quantisation raises
+ * tensor-core throughput, which makes the memory-bound SwiGLU steps
+ * relatively costlier ("Tile-Level Activation Overlap for Efficient LLM
+ * Inference", gist.science, section "Problem Statement"); they give no
+ * scaling scheme. Here each input is E4M3 values times one fp32 scale:
+ *   A = scale_a * A8,  W1 = scale_w1 * W1_8,  W2 = scale_w2 * W2_8,
+ *   Y = SiLU(A x W1) (.) (A x W2)   (bf16 output, fp32 accumulation; the
+ *   products scale_a * scale_w1 and scale_a * scale_w2 are formed in fp32).
+ * E4M3: 1 sign, 4 exponent (bias 7), 3 mantissa bits, max 448, no infinity.
+ *
+ * Packed FP8 weight: as for bf16 but with 128 one-byte K values per slice,
+ * viewed as bytes [Np/128][Kp/128][256][128], Kp = K rounded up to 128; size
+ * 2 * Np * Kp bytes. swiglu_pack_weights_fp8 takes W1_8, W2_8 as [K, N]
+ * E4M3 row-major device arrays. swiglu_forward_fp8 takes A8 [M, K] E4M3 and
+ * writes Y [M, N] bf16; M <= 64 uses the decode kernel, larger M the CTA-pair
+ * kernel. Requirements and errors as the bf16 calls, plus K a multiple of 16
+ * (UNSUPPORTED) and finite scales (INVALID_ARG).
+ */
+SWIGLU_API size_t swiglu_packed_weight_bytes_fp8(int64_t K, int64_t N);
+SWIGLU_API swiglu_status_t swiglu_pack_weights_fp8(const void* W1, const void* W2, void* Wpacked,
+                                                   int64_t K, int64_t N, swiglu_stream_t stream);
+SWIGLU_API swiglu_status_t swiglu_forward_fp8(const void* A, const void* Wpacked, void* Y,
+                                              int64_t M, int64_t K, int64_t N, float scale_a,
+                                              float scale_w1, float scale_w2,
+                                              swiglu_stream_t stream);
+
+/*
  * Allocation-free forward for callers that cannot call cudaMalloc: code that
  * runs while a stream is being captured into a CUDA graph (allocation is not
  * allowed there), serving runtimes that reserve all device memory for their

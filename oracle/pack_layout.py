@@ -37,20 +37,24 @@ def padded_k(k: int) -> int:
     return -(-k // PACK_BLOCK_K) * PACK_BLOCK_K
 
 
-def pack_reference(w1_bits: np.ndarray, w2_bits: np.ndarray) -> np.ndarray:
-    """Packed array [Np/128, Kp/64, 256, 64] (uint16 bf16 bits) from W1, W2 [K, N]."""
-    w1_bits = np.asarray(w1_bits, dtype=np.uint16)
-    w2_bits = np.asarray(w2_bits, dtype=np.uint16)
+def pack_reference(w1_bits: np.ndarray, w2_bits: np.ndarray, slice_k: int = PACK_BLOCK_K):
+    """Packed array [Np/128, Kp/slice_k, 256, slice_k] from W1, W2 [K, N] (bit arrays).
+
+    slice_k = 64 for bf16 (uint16 bits, 128-byte rows); the FP8 layout uses
+    slice_k = 128 (uint8 bits, also 128-byte rows).
+    """
+    w1_bits = np.asarray(w1_bits)
+    w2_bits = np.asarray(w2_bits)
     k_dim, n_dim = w1_bits.shape
     n_blocks = padded_n(n_dim) // PACK_BLOCK_N
-    k_slices = padded_k(k_dim) // PACK_BLOCK_K
-    out = np.zeros((n_blocks, k_slices, 2 * PACK_BLOCK_N, PACK_BLOCK_K), dtype=np.uint16)
+    k_slices = -(-k_dim // slice_k)
+    out = np.zeros((n_blocks, k_slices, 2 * PACK_BLOCK_N, slice_k), dtype=w1_bits.dtype)
     for j in range(n_blocks):
         n0 = j * PACK_BLOCK_N
         cols = min(PACK_BLOCK_N, n_dim - n0)          # real columns in this block
         for b in range(k_slices):
-            k0 = b * PACK_BLOCK_K
-            depth = min(PACK_BLOCK_K, k_dim - k0)     # real K values in this slice
+            k0 = b * slice_k
+            depth = min(slice_k, k_dim - k0)          # real K values in this slice
             # row i of the tile is weight column n0 + i, over k0 .. k0 + depth
             out[j, b, :cols, :depth] = w1_bits[k0:k0 + depth, n0:n0 + cols].T
             out[j, b, PACK_BLOCK_N:PACK_BLOCK_N + cols, :depth] = \

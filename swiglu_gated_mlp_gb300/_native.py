@@ -52,6 +52,13 @@ lib.swiglu_status_string.argtypes = [_int]
 lib.swiglu_status_string.restype = ctypes.c_char_p
 lib.swiglu_plan_string.argtypes = [_i64, _i64, _i64, _int, ctypes.c_char_p, _sz]
 lib.swiglu_plan_string.restype = _int
+lib.swiglu_packed_weight_bytes_fp8.argtypes = [_i64, _i64]
+lib.swiglu_packed_weight_bytes_fp8.restype = _sz
+lib.swiglu_pack_weights_fp8.argtypes = [_vp, _vp, _vp, _i64, _i64, _vp]
+lib.swiglu_pack_weights_fp8.restype = _int
+lib.swiglu_forward_fp8.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_float, ctypes.c_float,
+                                   ctypes.c_float, _vp]
+lib.swiglu_forward_fp8.restype = _int
 lib.swiglu_forward_noalloc.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp]
 lib.swiglu_forward_noalloc.restype = _int
 lib.swiglu_testing_inject_stall.argtypes = [_int, _u32]
@@ -165,6 +172,62 @@ def swiglu_forward(A: torch.Tensor, Wpacked: torch.Tensor, N: int, Y: torch.Tens
                    stream=None) -> torch.Tensor:
     """Y [M, N] = SiLU(A W1) * (A W2) from A [M, K] and the packed weight."""
     return swiglu_forward_variant(A, Wpacked, N, SWIGLU_VARIANT_AUTO, Y=Y, stream=stream)
+
+
+def _dev_fp8(t: torch.Tensor, name: str) -> None:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != torch.float8_e4m3fn:
+        raise ValueError(f"{name} must be float8_e4m3fn, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def swiglu_packed_weight_bytes_fp8(K: int, N: int) -> int:
+    return int(lib.swiglu_packed_weight_bytes_fp8(int(K), int(N)))
+
+
+def swiglu_pack_weights_fp8(W1: torch.Tensor, W2: torch.Tensor, Wpacked: torch.Tensor | None = None,
+                            stream=None) -> torch.Tensor:
+    """Packed FP8 gate/up weight (flat uint8 buffer) from E4M3 W1, W2 [K, N] (CUDA)."""
+    _dev_fp8(W1, "W1")
+    _dev_fp8(W2, "W2")
+    if W1.dim() != 2 or W1.shape != W2.shape:
+        raise ValueError("W1 and W2 must both be [K, N]")
+    K, N = W1.shape
+    if Wpacked is None:
+        Wpacked = torch.empty(swiglu_packed_weight_bytes_fp8(K, N), dtype=torch.uint8,
+                              device=W1.device)
+    if Wpacked.numel() * Wpacked.element_size() < swiglu_packed_weight_bytes_fp8(K, N):
+        raise ValueError("Wpacked is too small")
+    with _on_device(W1.device):
+        _check(lib.swiglu_pack_weights_fp8(W1.data_ptr(), W2.data_ptr(), Wpacked.data_ptr(), K, N,
+                                           _stream_handle(stream, W1.device)),
+               "swiglu_pack_weights_fp8")
+    return Wpacked
+
+
+def swiglu_forward_fp8(A: torch.Tensor, Wpacked: torch.Tensor, N: int, scale_a: float,
+                       scale_w1: float, scale_w2: float, Y: torch.Tensor | None = None,
+                       stream=None) -> torch.Tensor:
+    """Y [M, N] bf16 = SiLU(sa*A x s1*W1) * (sa*A x s2*W2) from E4M3 A [M, K] and the packed weight."""
+    _dev_fp8(A, "A")
+    if A.dim() != 2:
+        raise ValueError("A must be [M, K]")
+    M, K = A.shape
+    if Wpacked.numel() * Wpacked.element_size() < swiglu_packed_weight_bytes_fp8(K, N):
+        raise ValueError("Wpacked does not hold a packed FP8 weight for this K and N")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _dev_bf16(Y, "Y")
+    if tuple(Y.shape) != (M, N):
+        raise ValueError("Y must be [M, N]")
+    with _on_device(A.device):
+        _check(lib.swiglu_forward_fp8(A.data_ptr(), Wpacked.data_ptr(), Y.data_ptr(), M, K, N,
+                                      float(scale_a), float(scale_w1), float(scale_w2),
+                                      _stream_handle(stream, A.device)),
+               "swiglu_forward_fp8")
+    return Y
 
 
 def swiglu_forward_from_host(A_host: torch.Tensor, Wpacked: torch.Tensor, N: int,

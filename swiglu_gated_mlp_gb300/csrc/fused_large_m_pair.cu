@@ -53,9 +53,12 @@ __device__ __forceinline__ void pair_tile_coords(int t, int tiles_m, int tiles_n
   nb = r / gm;
 }
 
+template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     fused_large_m_pair_kernel(const __grid_constant__ LargeMParams p) {
   using C = PairCfg;
+  // K values per stage: 64 bf16 or 128 E4M3, a 128-byte row either way
+  constexpr int kBK = kFp8 ? kBlockK8 : kBlockK;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -78,7 +81,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int pair = static_cast<int>(cluster_id_x());
   const int pairs = static_cast<int>(cluster_count_x());
   const int num_tiles = p.tiles_m * p.tiles_n;
-  const int num_kb = (p.K + kBlockK - 1) / kBlockK;
+  const int num_kb = (p.K + kBK - 1) / kBK;
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
   // rank 0's full and tmem_empty barriers, as seen from either CTA of the pair
   const uint32_t full0_lead = mapa_shared(full0, 0);
@@ -134,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             if (leader) mbar_arrive_expect_tx(full0 + 8u * s, 2 * C::kStageBytes);
             const uint32_t fb = full0_lead + 8u * s;
-            tma_load_2d_pair(sA + s * C::kABytes, &p.tmap_a, fb, kb * kBlockK, m0);
+            tma_load_2d_pair(sA + s * C::kABytes, &p.tmap_a, fb, kb * kBK, m0);
             tma_load_3d_pair(sB + s * C::kBBytes, &p.tmap_w, fb, 0, wrow, wtile + kb);
             filled |= 1u << s;
             fill_ph = (fill_ph & ~(1u << s)) | (ph << s);
@@ -156,7 +159,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer (rank 0)
     if (leader && lane == 0) {
-      constexpr uint32_t kIdesc = idesc_bf16_f32(2 * kTileM, 2 * C::kBN);
+      constexpr uint32_t kIdesc = kFp8 ? idesc_e4m3_f32(2 * kTileM, 2 * C::kBN)
+                                       : idesc_bf16_f32(2 * kTileM, 2 * C::kBN);
       int s = 0;
       uint32_t ph = 0;
       int buf = 0;
@@ -175,8 +179,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t adesc = smem_desc_sw128(sA + s * C::kABytes);
           const uint64_t bdesc = smem_desc_sw128(sB + s * C::kBBytes);
 #pragma unroll
-          for (int k = 0; k < kBlockK / 16; ++k)
-            mma_bf16_pair(d, adesc + 2u * k, bdesc + 2u * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
+          for (int k = 0; k < 4; ++k) {  // four 32-byte K steps per 128-byte row
+            if constexpr (kFp8)
+              mma_e4m3_pair(d, adesc + 2u * k, bdesc + 2u * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
+            else
+              mma_bf16_pair(d, adesc + 2u * k, bdesc + 2u * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
+          }
           mma_commit_pair_multicast(empty0 + 8u * s, 0x3);  // frees the stage in both CTAs
           if (++s == C::kStages) {
             s = 0;
@@ -197,6 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int ew = warp - 2;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const float sg = kFp8 ? p.scale_gate : 1.0f, su = kFp8 ? p.scale_up : 1.0f;
     int buf = 0;
     uint32_t acc_ph = 0;
     int sbuf = 0;
@@ -234,8 +243,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int i0 = 8 * j + 2 * e;
-            w[e] = pack_bf16x2(silu_mul(__uint_as_float(g[i0]), __uint_as_float(u[i0])),
-                               silu_mul(__uint_as_float(g[i0 + 1]), __uint_as_float(u[i0 + 1])));
+            w[e] = pack_bf16x2(
+                silu_mul(sg * __uint_as_float(g[i0]), su * __uint_as_float(u[i0])),
+                silu_mul(sg * __uint_as_float(g[i0 + 1]), su * __uint_as_float(u[i0 + 1])));
           }
           st_shared_v4(row_addr + ((j ^ ((lane >> 1) & 3)) << 4), w[0], w[1], w[2], w[3]);
         }
@@ -286,14 +296,18 @@ cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribut
 }  // namespace
 
 cudaError_t configure_large_m_pair(int* max_pairs) {
-  cudaError_t e = cudaFuncSetAttribute(fused_large_m_pair_kernel,
+  cudaError_t e = cudaFuncSetAttribute(fused_large_m_pair_kernel<false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(PairCfg::kSmem));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fused_large_m_pair_kernel<true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(PairCfg::kSmem));
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pair_config(2, nullptr, attr, false);
   int clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&clusters, fused_large_m_pair_kernel, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&clusters, fused_large_m_pair_kernel<false>, &cfg);
   if (e != cudaSuccess) return e;
   *max_pairs = clusters;
   return cudaSuccess;
@@ -306,7 +320,8 @@ cudaError_t launch_large_m_pair(const LargeMParams& p, cudaStream_t stream) {
   if (p.grid < 2 || (p.grid % 2) != 0 || p.bn != PairCfg::kBN) return cudaErrorInvalidValue;
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pair_config(p.grid, stream, attr, pdl_enabled());
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, fused_large_m_pair_kernel, p);
+  const cudaError_t e = p.fp8 ? cudaLaunchKernelEx(&cfg, fused_large_m_pair_kernel<true>, p)
+                              : cudaLaunchKernelEx(&cfg, fused_large_m_pair_kernel<false>, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -40,14 +40,17 @@ constexpr int kMaxStages = 8;
 constexpr size_t kSmemLimit = 232448;
 constexpr int kBarBytes = 256;
 
+template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     fused_small_m_kernel(const __grid_constant__ SmallMParams p) {
+  // K values per stage: 64 bf16 or 128 E4M3, a 128-byte row either way
+  constexpr int kBK = kFp8 ? kBlockK8 : kBlockK;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const int mt = p.mt;
   const int stages = p.stages;
-  const uint32_t x_bytes = static_cast<uint32_t>(mt) * kBlockK * 2;
+  const uint32_t x_bytes = static_cast<uint32_t>(mt) * 128;
   const uint32_t stage_bytes = kWStageBytes + x_bytes;  // multiple of 1024 (mt % 8 == 0)
   const uint32_t s0 = smem_addr(smem);
   uint8_t* bar_ptr = smem + size_t(stages) * stage_bytes;
@@ -63,7 +66,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int num_kb = (p.K + kBlockK - 1) / kBlockK;
+  const int num_kb = (p.K + kBK - 1) / kBK;
   const int splits = p.splits > 1 ? p.splits : 1;
   const int nblk = blockIdx.x / splits;
   const int part = blockIdx.x % splits;  // the CTA's rank in its cluster when splits > 1
@@ -110,7 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           const uint32_t fb = full0 + 8u * s;
           const uint32_t sw = s0 + s * stage_bytes;
-          const int k0 = kb * kBlockK;
+          const int k0 = kb * kBK;
           mbar_arrive_expect_tx(fb, stage_bytes);
           tma_load_3d_hint(sw, &p.tmap_w, fb, 0, 0, wtile + kb, pol_w);  // one contiguous 32 KB tile
           tma_load_2d_hint(sw + kWStageBytes, &p.tmap_x, fb, k0, 0, pol_x);
@@ -130,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer -------
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(128, mt);
+      const uint32_t idesc = kFp8 ? idesc_e4m3_f32(128, mt) : idesc_bf16_f32(128, mt);
       const uint32_t d_gate = tmem_base;
       const uint32_t d_up = tmem_base + static_cast<uint32_t>(mt);
       int s = 0;
@@ -147,10 +150,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t udesc = smem_desc_sw128(sw + kWStageBytes / 2);      // up rows 128..255
         const uint64_t xdesc = smem_desc_sw128(sw + kWStageBytes);          // tokens
 #pragma unroll
-        for (int k = 0; k < kBlockK / 16; ++k) {
+        for (int k = 0; k < 4; ++k) {  // four 32-byte K steps per 128-byte row
           const uint32_t acc = (kb != kb_begin || k != 0) ? 1u : 0u;
-          mma_bf16(d_gate, gdesc + 2u * k, xdesc + 2u * k, idesc, acc);
-          mma_bf16(d_up, udesc + 2u * k, xdesc + 2u * k, idesc, acc);
+          if constexpr (kFp8) {
+            mma_e4m3(d_gate, gdesc + 2u * k, xdesc + 2u * k, idesc, acc);
+            mma_e4m3(d_up, udesc + 2u * k, xdesc + 2u * k, idesc, acc);
+          } else {
+            mma_bf16(d_gate, gdesc + 2u * k, xdesc + 2u * k, idesc, acc);
+            mma_bf16(d_up, udesc + 2u * k, xdesc + 2u * k, idesc, acc);
+          }
         }
         mma_commit(empty0 + 8u * s);
         if (++s == stages) {
@@ -195,6 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (ok) {
       tc_fence_after();
       __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(p.y);
+      const float sg = kFp8 ? p.scale_gate : 1.0f, su = kFp8 ? p.scale_up : 1.0f;
 #pragma unroll 1
       for (int mc = 0; mc < mt / 16; ++mc) {
         uint32_t g[16], u[16];
@@ -208,8 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 16; ++j) {
             const int m = mc * 16 + j;
             if (m < p.M)
-              y[static_cast<size_t>(m) * p.N + n] =
-                  __float2bfloat16_rn(silu_mul(__uint_as_float(g[j]), __uint_as_float(u[j])));
+              y[static_cast<size_t>(m) * p.N + n] = __float2bfloat16_rn(
+                  silu_mul(sg * __uint_as_float(g[j]), su * __uint_as_float(u[j])));
           }
         }
       }
@@ -238,6 +247,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         u.x += us.x; u.y += us.y; u.z += us.z; u.w += us.w;
       }
       const int n = nblk * kPackBlockN + r;  // N % 8 == 0: n < N implies n + 3 < N
+      if (kFp8) {
+        g.x *= p.scale_gate; g.y *= p.scale_gate; g.z *= p.scale_gate; g.w *= p.scale_gate;
+        u.x *= p.scale_up; u.y *= p.scale_up; u.z *= p.scale_up; u.w *= p.scale_up;
+      }
       if (n < p.N) {
         uint2 v;
         v.x = pack_bf16x2(silu_mul(g.x, u.x), silu_mul(g.y, u.y));
@@ -271,14 +284,20 @@ size_t small_m_smem_bytes(int mt, int stages) {
   return 1024 + size_t(stages) * (kWStageBytes + size_t(mt) * kBlockK * 2) + kBarBytes;
 }
 
-cudaError_t configure_small_m() {
-  cudaError_t e = cudaFuncSetAttribute(fused_small_m_kernel,
+template <bool kFp8>
+cudaError_t configure_small_m_t() {
+  cudaError_t e = cudaFuncSetAttribute(fused_small_m_kernel<kFp8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemLimit));
   if (e == cudaSuccess)  // all of the unified L1/shared array as shared memory (2 CTAs may share an SM)
-    e = cudaFuncSetAttribute(fused_small_m_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             100);
+    e = cudaFuncSetAttribute(fused_small_m_kernel<kFp8>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   return e;
+}
+
+cudaError_t configure_small_m() {
+  const cudaError_t e = configure_small_m_t<false>();
+  return e != cudaSuccess ? e : configure_small_m_t<true>();
 }
 
 cudaError_t static_scratch_address(uint32_t** out) {
@@ -304,7 +323,7 @@ int small_m_max_clusters(int splits) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, fused_small_m_kernel, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&clusters, fused_small_m_kernel<false>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -315,7 +334,8 @@ cudaError_t launch_small_m(const SmallMParams& p, cudaStream_t stream) {
   if (p.stages < 2 || p.stages > kMaxStages || p.mt < 16 || p.mt > 256 || (p.mt % 16) != 0)
     return cudaErrorInvalidValue;
   const int splits = p.splits > 1 ? p.splits : 1;
-  const int num_kb = (p.K + kBlockK - 1) / kBlockK;
+  const int bk = p.fp8 ? kBlockK8 : kBlockK;
+  const int num_kb = (p.K + bk - 1) / bk;
   if (splits > 1 &&
       (splits > 8 || (kPackBlockN % (4 * splits)) != 0 || splits > num_kb || p.mt > 128 ||
        size_t(2) * p.mt * kPackBlockN * 4 > size_t(p.stages) * (kWStageBytes + size_t(p.mt) * kBlockK * 2) ||
@@ -335,7 +355,8 @@ cudaError_t launch_small_m(const SmallMParams& p, cudaStream_t stream) {
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = splits > 1 ? 2 : 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, fused_small_m_kernel, p);
+  const cudaError_t e = p.fp8 ? cudaLaunchKernelEx(&cfg, fused_small_m_kernel<true>, p)
+                              : cudaLaunchKernelEx(&cfg, fused_small_m_kernel<false>, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -11,6 +11,7 @@ namespace swg {
 
 constexpr int kPackBlockN = 128;  // columns per gate/up block of the packed weight
 constexpr int kBlockK = 64;       // K elements per pipeline stage (128 B rows, 128-B swizzle)
+constexpr int kBlockK8 = 128;     // the same 128-byte rows for one-byte (FP8 E4M3) elements
 constexpr int kTileM = 128;       // tokens per large-M tile (MMA M)
 constexpr int kThreads = 192;     // 6 warps: TMA producer, MMA issuer, 4 epilogue warps
 
@@ -22,6 +23,8 @@ struct LargeMParams {
   int tiles_m, tiles_n, group_m;
   int bn;    // output columns per tile: 32, 64 or 128 (MMA N = 2 * bn)
   int grid;  // persistent CTAs
+  int fp8;   // E4M3 inputs (pair kernel): gate and up accumulators are scaled by
+  float scale_gate, scale_up;  // scale_a * scale_w1 and scale_a * scale_w2 in the epilogue
   uint32_t* status;
   uint64_t timeout_ns;
   int inject_stall;
@@ -36,6 +39,8 @@ struct SmallMParams {
   int stages;  // pipeline depth
   int grid;    // one CTA per 128-column block and K part (splits)
   int splits;  // K parts per column block (<= 1: none); > 1: clusters of `splits` CTAs
+  int fp8;     // E4M3 inputs: accumulators are scaled by scale_gate / scale_up
+  float scale_gate, scale_up;
   uint32_t* status;
   uint64_t timeout_ns;
   int inject_stall;
@@ -83,5 +88,7 @@ int small_m_max_clusters(int splits);
 
 cudaError_t launch_pack(const void* w1, const void* w2, void* wp, int K, int N,
                         cudaStream_t stream);
+cudaError_t launch_pack_fp8(const void* w1, const void* w2, void* wp, int K, int N,
+                            cudaStream_t stream);
 
 }  // namespace swg

@@ -1,14 +1,16 @@
 // Packs W1, W2 [K, N] (N contiguous) into the tile-major, block-interleaved
-// weight the fused kernels stream. Viewed as bf16 [Np/128][Kp/64][256][64]:
-//   Wp[j][b][i][t]       = W1[64b + t][128j + i]   (i < 128, gate)
-//   Wp[j][b][128 + i][t] = W2[64b + t][128j + i]   (i < 128, up)
-// zero where a column is >= N or a K index is >= K. Every [256][64] tile (32 KB)
+// weight the fused kernels stream. For bf16 elements, viewed as
+// [Np/128][Kp/64][256][64]; for FP8 (one byte) as [Np/128][Kp/128][256][128]:
+//   Wp[j][b][i][t]       = W1[S b + t][128j + i]   (i < 128, gate)
+//   Wp[j][b][128 + i][t] = W2[S b + t][128j + i]   (i < 128, up)
+// with S = 64 or 128 values per K slice (a row is 128 bytes either way), zero
+// where a column is >= N or a K index is >= K. Every [256][S] tile (32 KB)
 // is contiguous, so each TMA box the kernels load is one contiguous span of
 // memory. The pages fuse W1 and W2 into one K x 2N matrix ahead of time
 // ("Tile-Level Activation Overlap for Efficient LLM Inference", gist.science,
 // section "Methodology / Kernel-2"); this is that step, with 128-column blocks
 // instead of single-column interleave. It runs once per weight set: one CTA
-// per tile, a transpose through shared memory.
+// per tile, a transpose through shared memory; the bits are copied unchanged.
 #include "kernels.h"
 
 namespace swg {
@@ -16,26 +18,28 @@ namespace {
 
 constexpr int kTileRows = 2 * kPackBlockN;  // 256 packed rows: gate block, then up block
 
+template <typename T, int S>
 __global__ void __launch_bounds__(256)
-    pack_kernel(const uint16_t* __restrict__ w1, const uint16_t* __restrict__ w2,
-                uint16_t* __restrict__ wp, int K, int N, int k_slices) {
-  __shared__ uint16_t tile[kBlockK][kTileRows + 2];  // [t][i]; +2 keeps the column reads conflict-free
-  const int b = blockIdx.x;                           // K slice
-  const int j = blockIdx.y;                           // column block
-  const int k0 = b * kBlockK, n0 = j * kPackBlockN;
+    pack_kernel(const T* __restrict__ w1, const T* __restrict__ w2, T* __restrict__ wp, int K,
+                int N, int k_slices) {
+  // [t][i]; the padding keeps the column reads conflict-free
+  __shared__ T tile[S][kTileRows + 4 / sizeof(T)];
+  const int b = blockIdx.x;  // K slice
+  const int j = blockIdx.y;  // column block
+  const int k0 = b * S, n0 = j * kPackBlockN;
   // load: for each k, 128 consecutive columns of W1 then of W2 (coalesced)
-  for (int idx = threadIdx.x; idx < kBlockK * kTileRows; idx += blockDim.x) {
+  for (int idx = threadIdx.x; idx < S * kTileRows; idx += blockDim.x) {
     const int t = idx / kTileRows, i = idx % kTileRows;
     const int k = k0 + t, n = n0 + (i % kPackBlockN);
-    const uint16_t* __restrict__ src = i < kPackBlockN ? w1 : w2;
-    tile[t][i] = (k < K && n < N) ? src[static_cast<size_t>(k) * N + n] : uint16_t(0);
+    const T* __restrict__ src = i < kPackBlockN ? w1 : w2;
+    tile[t][i] = (k < K && n < N) ? src[static_cast<size_t>(k) * N + n] : T(0);
   }
   __syncthreads();
-  // store: the tile's 256 rows of 64 K values, contiguous
-  uint16_t* __restrict__ out =
-      wp + (static_cast<size_t>(j) * k_slices + b) * (static_cast<size_t>(kTileRows) * kBlockK);
-  for (int idx = threadIdx.x; idx < kBlockK * kTileRows; idx += blockDim.x) {
-    const int i = idx / kBlockK, t = idx % kBlockK;
+  // store: the tile's 256 rows of S K values, contiguous
+  T* __restrict__ out =
+      wp + (static_cast<size_t>(j) * k_slices + b) * (static_cast<size_t>(kTileRows) * S);
+  for (int idx = threadIdx.x; idx < S * kTileRows; idx += blockDim.x) {
+    const int i = idx / S, t = idx % S;
     out[idx] = tile[t][i];
   }
 }
@@ -47,9 +51,20 @@ cudaError_t launch_pack(const void* w1, const void* w2, void* wp, int K, int N,
   const int n_blocks = (N + kPackBlockN - 1) / kPackBlockN;
   const int k_slices = (K + kBlockK - 1) / kBlockK;
   const dim3 grid(k_slices, n_blocks);
-  pack_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(w1),
-                                        static_cast<const uint16_t*>(w2),
-                                        static_cast<uint16_t*>(wp), K, N, k_slices);
+  pack_kernel<uint16_t, kBlockK><<<grid, 256, 0, stream>>>(
+      static_cast<const uint16_t*>(w1), static_cast<const uint16_t*>(w2),
+      static_cast<uint16_t*>(wp), K, N, k_slices);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_fp8(const void* w1, const void* w2, void* wp, int K, int N,
+                            cudaStream_t stream) {
+  const int n_blocks = (N + kPackBlockN - 1) / kPackBlockN;
+  const int k_slices = (K + kBlockK8 - 1) / kBlockK8;
+  const dim3 grid(k_slices, n_blocks);
+  pack_kernel<uint8_t, kBlockK8><<<grid, 256, 0, stream>>>(
+      static_cast<const uint8_t*>(w1), static_cast<const uint8_t*>(w2),
+      static_cast<uint8_t*>(wp), K, N, k_slices);
   return cudaGetLastError();
 }
 

@@ -3,6 +3,7 @@
 #include "swiglu.h"
 
 #include <atomic>
+#include <cmath>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -131,6 +132,7 @@ swiglu_status_t device_state(DeviceState** out) {
 // host cost on every call. Entries are keyed on every encoded field.
 struct TmapKey {
   const void* base;
+  int dtype;
   cuuint64_t dims[3];
   cuuint64_t strides[2];
   cuuint32_t box[3];
@@ -149,10 +151,12 @@ struct TmapCache {
 thread_local TmapCache t_tmap_cache;
 
 bool encode_cached(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
-                   const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swizzle) {
+                   const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swizzle,
+                   CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   TmapKey k;
   std::memset(&k, 0, sizeof(k));
   k.base = base;
+  k.dtype = static_cast<int>(dtype);
   k.rank = rank;
   k.swizzle = static_cast<int>(swizzle);
   for (int i = 0; i < rank; ++i) {
@@ -168,7 +172,7 @@ bool encode_cached(CUtensorMap* map, const void* base, int rank, const cuuint64_
     }
   }
   cuuint32_t estr[3] = {1, 1, 1};
-  if (g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base),
+  if (g_encode(map, dtype, rank, const_cast<void*>(base),
                const_cast<cuuint64_t*>(dims), const_cast<cuuint64_t*>(strides),
                const_cast<cuuint32_t*>(box), estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -182,11 +186,12 @@ bool encode_cached(CUtensorMap* map, const void* base, int rank, const cuuint64_
 
 bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
-               CUtensorMapSwizzle swizzle) {
+               CUtensorMapSwizzle swizzle,
+               CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {row_bytes};
   const cuuint32_t box[2] = {box_inner, box_outer};
-  return encode_cached(map, base, 2, dims, strides, box, swizzle);
+  return encode_cached(map, base, 2, dims, strides, box, swizzle, dtype);
 }
 
 // The packed weight as a 3-D tensor {64 K values, 256 rows, tiles}: every tile
@@ -201,6 +206,19 @@ bool encode_packed_w(CUtensorMap* map, const void* base, int64_t K, int64_t N, u
   return encode_cached(map, base, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// The FP8 packed weight: {128 one-byte K values, 256 rows, tiles}, 32 KB tiles.
+int64_t k_slices8(int64_t k) { return (k + swg::kBlockK8 - 1) / swg::kBlockK8; }
+
+bool encode_packed_w8(CUtensorMap* map, const void* base, int64_t K, int64_t N, uint32_t rows) {
+  const int64_t tiles = (padded_n(N) / swg::kPackBlockN) * k_slices8(K);
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(swg::kBlockK8), 2u * swg::kPackBlockN,
+                              static_cast<cuuint64_t>(tiles)};
+  const cuuint64_t strides[2] = {swg::kBlockK8, 2u * swg::kPackBlockN * swg::kBlockK8};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(swg::kBlockK8), rows, 1};
+  return encode_cached(map, base, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_DATA_TYPE_UINT8);
+}
+
 struct Plan {
   int variant = SWIGLU_VARIANT_AUTO;
   int bn = 0, stages = 0, tiles_m = 0, tiles_n = 0, group_m = 0, tiles = 0, grid = 0, mt = 0;
@@ -209,7 +227,9 @@ struct Plan {
 
 // `d` may be null (allocation-free entry point): no SM count, no cluster data.
 swiglu_status_t make_plan(int64_t M, int64_t K, int64_t N, int variant, const DeviceState* d,
-                          Plan* pl) {
+                          Plan* pl, int elem_bytes = 2) {
+  // 128-byte K slices: 64 bf16 or 128 E4M3 values
+  const int64_t kslices = elem_bytes == 1 ? k_slices8(K) : k_slices(K);
   const int sm_count = d ? d->sm_count : 0;
   const int max_pairs = d ? d->max_pairs : 0;
   if (variant < SWIGLU_VARIANT_AUTO || variant > SWIGLU_VARIANT_SEQUENTIAL)
@@ -246,7 +266,7 @@ swiglu_status_t make_plan(int64_t M, int64_t K, int64_t N, int variant, const De
     // (only for few tokens: with more, the partials' exchange costs more than it saves)
     if (d && pl->mt <= 64 && int64_t(pl->mt) * 1024 <= pl->stages * stage_bytes) {
       for (int s : {8, 4, 2}) {
-        if (pl->tiles * s <= sm_count && s <= k_slices(K) && d->small_clusters[s] >= pl->tiles) {
+        if (pl->tiles * s <= sm_count && s <= kslices && d->small_clusters[s] >= pl->tiles) {
           pl->splits = s;
           break;
         }
@@ -277,7 +297,7 @@ swiglu_status_t make_plan(int64_t M, int64_t K, int64_t N, int variant, const De
     const int64_t pm = (M + 2 * swg::kTileM - 1) / (2 * swg::kTileM);  // 256-row tiles
     const int64_t ptiles = pm * (np / swg::kPackBlockN);
     if (ptiles > 2147483647) return SWIGLU_ERR_UNSUPPORTED;
-    int64_t group = (48ll << 20) / (int64_t(2 * swg::kTileM) * K * 2);
+    int64_t group = (48ll << 20) / (int64_t(2 * swg::kTileM) * K * elem_bytes);
     if (group < 1) group = 1;
     if (group > pm) group = pm;
     pl->bn = swg::kPackBlockN;
@@ -633,6 +653,110 @@ swiglu_status_t swiglu_forward_noalloc(const void* A, const void* Wpacked, void*
   }
   if (status_out && cudaMemcpyAsync(status_out, s->scratch, swg::kStatusWords * sizeof(uint32_t),
                                     cudaMemcpyDeviceToHost, cs) != cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_ERR_CUDA;
+  }
+  return SWIGLU_OK;
+}
+
+size_t swiglu_packed_weight_bytes_fp8(int64_t K, int64_t N) {
+  if (K <= 0 || N <= 0 || K > kMaxKN || N > kMaxKN) return 0;
+  return size_t(2) * size_t(padded_n(N)) * size_t(k_slices8(K) * swg::kBlockK8);
+}
+
+swiglu_status_t swiglu_pack_weights_fp8(const void* W1, const void* W2, void* Wpacked, int64_t K,
+                                        int64_t N, swiglu_stream_t stream) {
+  swiglu_status_t st = check_shape(0, K, N);
+  if (st != SWIGLU_OK) return st;
+  if ((K % 16) != 0) return SWIGLU_ERR_UNSUPPORTED;  // 16-byte rows of one-byte values
+  if (!W1 || !W2 || !Wpacked) return SWIGLU_ERR_INVALID_ARG;
+  if (!aligned16(W1) || !aligned16(W2) || !aligned16(Wpacked)) return SWIGLU_ERR_INVALID_ARG;
+  const size_t w_bytes = size_t(K) * size_t(N);
+  const size_t p_bytes = swiglu_packed_weight_bytes_fp8(K, N);
+  if (overlaps(Wpacked, p_bytes, W1, w_bytes) || overlaps(Wpacked, p_bytes, W2, w_bytes))
+    return SWIGLU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != SWIGLU_OK) return st;
+  if (swg::launch_pack_fp8(W1, W2, Wpacked, static_cast<int>(K), static_cast<int>(N),
+                           reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_ERR_CUDA;
+  }
+  return SWIGLU_OK;
+}
+
+swiglu_status_t swiglu_forward_fp8(const void* A, const void* Wpacked, void* Y, int64_t M,
+                                   int64_t K, int64_t N, float scale_a, float scale_w1,
+                                   float scale_w2, swiglu_stream_t stream) {
+  swiglu_status_t st = check_shape(M, K, N);
+  if (st != SWIGLU_OK) return st;
+  if ((K % 16) != 0) return SWIGLU_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale_a) || !std::isfinite(scale_w1) || !std::isfinite(scale_w2))
+    return SWIGLU_ERR_INVALID_ARG;
+  if (M == 0) return SWIGLU_OK;
+  if (!A || !Wpacked || !Y) return SWIGLU_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(Wpacked) || !aligned16(Y)) return SWIGLU_ERR_INVALID_ARG;
+  const size_t a_bytes = size_t(M) * size_t(K), y_bytes = size_t(M) * size_t(N) * 2;
+  if (overlaps(Y, y_bytes, A, a_bytes) ||
+      overlaps(Y, y_bytes, Wpacked, swiglu_packed_weight_bytes_fp8(K, N)))
+    return SWIGLU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != SWIGLU_OK) return st;
+  // Decode sizes take the decode kernel, the rest CTA pairs (the two FP8 kernels).
+  Plan pl;
+  const bool small = M <= 64;
+  st = make_plan(M, K, N, small ? SWIGLU_VARIANT_SMALL_M : SWIGLU_VARIANT_LARGE_M_PAIR, d, &pl, 1);
+  if (st != SWIGLU_OK) return st;
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const float sg = scale_a * scale_w1, su = scale_a * scale_w2;
+  cudaError_t err;
+  if (small) {
+    swg::SmallMParams p{};
+    if (!encode_2d(&p.tmap_x, A, K, M, K, swg::kBlockK8, pl.mt, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_DATA_TYPE_UINT8) ||
+        !encode_packed_w8(&p.tmap_w, Wpacked, K, N, 2 * swg::kPackBlockN))
+      return SWIGLU_ERR_CUDA;
+    p.y = Y;
+    p.M = static_cast<int>(M);
+    p.K = static_cast<int>(K);
+    p.N = static_cast<int>(N);
+    p.mt = pl.mt;
+    p.stages = pl.stages;
+    p.grid = pl.grid;
+    p.splits = pl.splits;
+    p.fp8 = 1;
+    p.scale_gate = sg;
+    p.scale_up = su;
+    p.status = d->status;
+    p.timeout_ns = g_timeout_ns.load();
+    p.inject_stall = g_inject.load();
+    err = swg::launch_small_m(p, cs);
+  } else {
+    swg::LargeMParams p{};
+    if (!encode_2d(&p.tmap_a, A, K, M, K, swg::kBlockK8, swg::kTileM, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_DATA_TYPE_UINT8) ||
+        !encode_packed_w8(&p.tmap_w, Wpacked, K, N, pl.bn) ||
+        !encode_2d(&p.tmap_y, Y, N, M, N * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+      return SWIGLU_ERR_CUDA;
+    p.M = static_cast<int>(M);
+    p.K = static_cast<int>(K);
+    p.N = static_cast<int>(N);
+    p.tiles_m = pl.tiles_m;
+    p.tiles_n = pl.tiles_n;
+    p.group_m = pl.group_m;
+    p.bn = pl.bn;
+    p.grid = pl.grid;
+    p.fp8 = 1;
+    p.scale_gate = sg;
+    p.scale_up = su;
+    p.status = d->status;
+    p.timeout_ns = g_timeout_ns.load();
+    p.inject_stall = g_inject.load();
+    err = swg::launch_large_m_pair(p, cs);
+  }
+  if (err != cudaSuccess) {
     cudaGetLastError();
     return SWIGLU_ERR_CUDA;
   }

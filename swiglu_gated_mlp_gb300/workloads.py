@@ -98,3 +98,30 @@ def sample_rows(M: int, count: int, seed: int) -> np.ndarray:
     rng = np.random.default_rng(seed + 7919)
     inner = rng.choice(np.arange(1, M - 1), size=max(count - 2, 0), replace=False)
     return np.unique(np.concatenate([[0, M - 1], inner]).astype(np.int64))
+
+
+def make_inputs_fp8(M: int, K: int, N: int, seed: int):
+    """FP8 (E4M3) inputs with one fp32 scale per tensor, for the FP8 path.
+
+    The same seeded draws as ``make_inputs`` (float32, before any rounding),
+    each quantised as x ~= s * q with s = max|x| / 448 and q = RNE_E4M3(x / s).
+    Returns (A8 [M,K], W1_8 [K,N], W2_8 [K,N]) as CPU float8_e4m3fn tensors and
+    the scales (s_a, s_1, s_2) as Python floats (exact fp32 values).
+    """
+    g = torch.Generator().manual_seed(int(seed))
+    a = torch.randn(M, K, generator=g, dtype=torch.float32)
+    scale = 1.0 / math.sqrt(K)
+    w1 = torch.randn(K, N, generator=g, dtype=torch.float32) * scale
+    w2 = torch.randn(K, N, generator=g, dtype=torch.float32) * scale
+    out, scales = [], []
+    for x in (a, w1, w2):
+        s = torch.clamp(x.abs().max() / 448.0, min=1e-30).to(torch.float32)
+        out.append((x / s).to(torch.float8_e4m3fn).contiguous())
+        scales.append(float(s))
+    return out[0], out[1], out[2], tuple(scales)
+
+
+def fp8_bits(t: torch.Tensor) -> np.ndarray:
+    """The raw E4M3 bit patterns of a CPU float8 tensor as a numpy uint8 array."""
+    assert t.dtype == torch.float8_e4m3fn
+    return t.detach().cpu().contiguous().view(torch.uint8).numpy()

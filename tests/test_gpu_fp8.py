@@ -1,0 +1,90 @@
+"""Parity of the FP8 (E4M3) path with the FP8 oracle (needs a GB300).
+
+Inputs are E4M3 values with one fp32 scale per tensor (the reading taken for
+the pages' remark on FP8 quantisation, "Problem Statement"); the oracle
+computes Y in float64 from the exact decoded values. Same pass rule as the
+bf16 path: |y - ref| <= 1e-2 |ref| + 1e-3 for every compared element.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import compare, pack_layout
+from oracle.fp8 import swiglu_f64_fp8
+from swiglu_gated_mlp_gb300.workloads import (WORKLOADS, bf16_bits, fp8_bits, make_inputs_fp8,
+                                              sample_rows)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def native(native_lib):
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return native_lib
+
+
+def run_fp8(native, M, K, N, seed, rows=None):
+    a8, w18, w28, (sa, s1, s2) = make_inputs_fp8(M, K, N, seed)
+    wp = native.swiglu_pack_weights_fp8(w18.cuda(), w28.cuda())
+    y = native.swiglu_forward_fp8(a8.cuda(), wp, N, sa, s1, s2)
+    native.swiglu_check_device_status()
+    yb = bf16_bits(y.cpu())
+    if rows is not None:
+        yb = yb[rows]
+    ref = swiglu_f64_fp8(fp8_bits(a8), fp8_bits(w18), fp8_bits(w28), sa, s1, s2, rows=rows)
+    rep = compare.report(yb, ref)
+    assert rep["nonfinite"] == 0, rep
+    assert rep["tolerance_pass"], rep
+    return rep
+
+
+@pytest.mark.parametrize("K,N", [(128, 128), (144, 136), (400, 264), (896, 4864)])
+def test_fp8_pack_is_bit_exact(native, K, N):
+    _, w18, w28, _ = make_inputs_fp8(1, K, N, seed=K + N)
+    wp = native.swiglu_pack_weights_fp8(w18.cuda(), w28.cuda())
+    torch.cuda.synchronize()
+    want = pack_layout.pack_reference(fp8_bits(w18), fp8_bits(w28), slice_k=128)
+    got = wp.cpu().numpy().reshape(-1)
+    assert got.size == native.swiglu_packed_weight_bytes_fp8(K, N)
+    assert np.array_equal(got, want.reshape(-1))
+
+
+# decode kernel (M <= 64), with and without K split over clusters, and the
+# CTA-pair kernel (M > 64); K multiples of 16 with ragged 128-value slices
+CASES = [
+    (1, 128, 128), (16, 3584, 1280), (16, 144, 136), (33, 400, 264), (64, 896, 4864),
+    (16, 896, 4864), (65, 256, 512), (100, 400, 264), (256, 1024, 1024), (300, 512, 1000),
+    (1000, 2048, 768),
+]
+
+
+@pytest.mark.parametrize("M,K,N", CASES)
+def test_fp8_forward_matches_oracle(native, M, K, N):
+    run_fp8(native, M, K, N, seed=M + 3 * K + N)
+
+
+@pytest.mark.parametrize("name", ["qwen2.5-7b-decode-m16", "qwen2.5-7b-prefill-m4096"])
+def test_fp8_full_size_workloads(native, name):
+    w = WORKLOADS[name]
+    rows = sample_rows(w.M, 64, seed=w.seed)
+    rep = run_fp8(native, w.M, w.K, w.N, seed=w.seed, rows=rows)
+    assert rep["mismatch_rate"] == 0.0
+
+
+def test_fp8_zero_activations_give_zero(native):
+    _, w18, w28, (_, s1, s2) = make_inputs_fp8(1, 256, 384, seed=9)
+    wp = native.swiglu_pack_weights_fp8(w18.cuda(), w28.cuda())
+    for M in (16, 200):
+        a8 = torch.zeros(M, 256, dtype=torch.float8_e4m3fn, device="cuda")
+        y = native.swiglu_forward_fp8(a8, wp, 384, 1.0, s1, s2)
+        torch.cuda.synchronize()
+        assert torch.count_nonzero(y.float()) == 0
+
+
+def test_fp8_rejects_bad_arguments(native):
+    lib = native.lib
+    fake = 0x10000
+    assert lib.swiglu_forward_fp8(fake, fake * 64, fake * 256, 4, 72, 64, 1.0, 1.0, 1.0,
+                                  None) == native.SWIGLU_ERR_UNSUPPORTED  # K % 16
+    assert lib.swiglu_forward_fp8(fake, fake * 64, fake * 256, 4, 64, 64, float("nan"), 1.0,
+                                  1.0, None) == native.SWIGLU_ERR_INVALID_ARG

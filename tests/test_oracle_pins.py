@@ -300,3 +300,66 @@ def test_pack_layout_matches_elementwise_definition():
                     src = w1b if i < 128 else w2b
                     want = src[k, n] if (k < 72 and n < 136) else 0
                     assert p[j, b, i, t] == want
+
+
+# ------------------------------------------------------------- FP8 path ----
+
+def test_e4m3_decode_known_patterns():
+    from oracle.fp8 import e4m3_bits_to_f64
+    bits = np.array([0x00, 0x38, 0xB8, 0x7E, 0x08, 0x01, 0x07, 0x80, 0x40], dtype=np.uint8)
+    v = e4m3_bits_to_f64(bits)
+    assert v.tolist()[:7] == [0.0, 1.0, -1.0, 448.0, 2.0 ** -6, 2.0 ** -9, 7 * 2.0 ** -9]
+    assert v[7] == 0.0 and np.signbit(v[7]) and v[8] == 2.0
+    assert np.isnan(e4m3_bits_to_f64(np.array([0x7F, 0xFF], dtype=np.uint8))).all()
+
+
+def test_e4m3_decode_agrees_with_torch_on_all_patterns():
+    from oracle.fp8 import e4m3_bits_to_f64
+    bits = np.arange(256, dtype=np.uint8)
+    want = torch.from_numpy(bits).view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    got = e4m3_bits_to_f64(bits)
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok], want[ok].astype(np.float64))
+
+
+def test_fp8_reference_reduces_to_the_bf16_reference():
+    # with unit scales, E4M3 values are exact in bf16: both references agree exactly
+    from oracle.fp8 import e4m3_bits_to_f64, swiglu_f64_fp8
+    rng = np.random.default_rng(3)
+    a8 = rng.integers(0, 256, size=(5, 48), dtype=np.uint8)
+    w18 = rng.integers(0, 256, size=(48, 24), dtype=np.uint8)
+    w28 = rng.integers(0, 256, size=(48, 24), dtype=np.uint8)
+    for arr in (a8, w18, w28):                     # no NaN patterns
+        arr[(arr & 0x7F) == 0x7F] = 0x38
+    got = swiglu_f64_fp8(a8, w18, w28, 1.0, 1.0, 1.0)
+    to_bf16 = lambda b: f64_to_bf16_bits(e4m3_bits_to_f64(b))
+    want = swiglu_f64(to_bf16(a8), to_bf16(w18), to_bf16(w28))
+    assert np.array_equal(got, want)
+
+
+def test_fp8_reference_scales():
+    from oracle.fp8 import swiglu_f64_fp8
+    rng = np.random.default_rng(4)
+    a8 = rng.integers(0, 0x70, size=(3, 32), dtype=np.uint8)
+    w18 = rng.integers(0, 0x70, size=(32, 16), dtype=np.uint8)
+    w28 = rng.integers(0x80, 0xF0, size=(32, 16), dtype=np.uint8)
+    y = swiglu_f64_fp8(a8, w18, w28, 0.5, 0.25, 0.125)
+    # Y is linear in the up scale (exact for a power of two)
+    assert np.array_equal(swiglu_f64_fp8(a8, w18, w28, 0.5, 0.25, 0.25), 2.0 * y)
+    # rows subset
+    assert np.array_equal(swiglu_f64_fp8(a8, w18, w28, 0.5, 0.25, 0.125, rows=[2, 0]), y[[2, 0]])
+
+
+def test_fp8_pack_layout_uses_128_value_slices():
+    rng = np.random.default_rng(5)
+    w1 = rng.integers(0, 256, size=(200, 136), dtype=np.uint8)
+    w2 = rng.integers(0, 256, size=(200, 136), dtype=np.uint8)
+    p = pack_layout.pack_reference(w1, w2, slice_k=128)
+    assert p.shape == (2, 2, 256, 128) and p.dtype == np.uint8
+    for n in (0, 127, 128, 135):
+        j, i = divmod(n, 128)
+        for k in (0, 127, 128, 199):
+            b, t = divmod(k, 128)
+            assert p[j, b, i, t] == w1[k, n] and p[j, b, 128 + i, t] == w2[k, n]
+    assert not p[1, :, 8:128].any() and not p[:, 1, :, 72:].any()
