@@ -48,9 +48,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from swiglu_gated_mlp_gb300.workloads import (WORKLOADS, Workload, bf16_bits,  # noqa: E402
-                                              make_inputs_fp8, make_workload_inputs, sweep_32b)
+                                              make_inputs, make_inputs_fp8, make_workload_inputs,
+                                              sweep_32b)
 
 METRIC = "fused SwiGLU-GEMM TFLOP/s (4·M·K·N) and % of GB300 dense BF16 peak"
+METRIC_DOWN = "MLP down-projection TFLOP/s (2·M·N·H), Out = Y·W3 + R"
 DEFAULT_WORKLOAD = "qwen2.5-7b-decode-m16"
 # swiglu_forward_variant's kernel choice (auto = what swiglu_forward does)
 VARIANTS = {"auto": 0, "large": 1, "small": 2, "pair": 3, "sequential": 4}
@@ -218,9 +220,22 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     M, K, N = w.M, w.K, w.N
 
     fp8 = args.dtype == "fp8"
+    down = args.op == "down"
+    if down and fp8:
+        raise SystemExit("--op down runs in bf16 only")
     elem = 1 if fp8 else 2
+    flops = w.flops
     alg_bytes = elem * M * K + 2 * elem * K * N + 2 * M * N  # A, W1 and W2 once, Y (bf16)
-    if fp8:
+    if down:
+        # Out [M, H] = Y [M, N] x W3 [N, H] + R at this workload's MLP shape (H = K)
+        H = K
+        flops = 2 * M * N * H
+        alg_bytes = 2 * M * N + 2 * N * H + 2 * 2 * M * H  # Y, W3 once, R read, Out written
+        y_cpu, w3_cpu, _ = make_inputs(M, N, H, w.seed)
+        r_cpu = make_inputs(M, H, 8, w.seed + 1)[0]
+        wp0 = sg.swiglu_pack_down_weights(w3_cpu.to(dev))
+        a_cpu = y_cpu
+    elif fp8:
         a_cpu, w1_cpu, w2_cpu, (s_a, s_1, s_2) = make_inputs_fp8(M, K, N, w.seed)
         wp0 = sg.swiglu_pack_weights_fp8(w1_cpu.to(dev), w2_cpu.to(dev))
     else:
@@ -235,15 +250,24 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     wps = [wp0] + [wp0.clone() for _ in range(copies - 1)]
     a0 = a_cpu.to(dev)
     As = [a0] + [a0.clone() for _ in range(copies - 1)]
-    Ys = [torch.empty(M, N, dtype=torch.bfloat16, device=dev) for _ in range(copies)]
+    out_cols = K if down else N
+    Ys = [torch.empty(M, out_cols, dtype=torch.bfloat16, device=dev) for _ in range(copies)]
+    if down:
+        r0 = r_cpu.to(dev)
+        Rs = [r0] + [r0.clone() for _ in range(copies - 1)]
     variant = VARIANTS[args.variant]
-    plan = sg.swiglu_plan_string(M, K, N, variant) if not fp8 else (
-        "fp8 " + ("small_m" if M <= 64 else "large_m_pair"))
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    down_small = M <= 64 or (M <= 128 and 2 * (-(-K // 256)) <= sms)
+    plan = (("down small_m" if down_small else "down large_m_pair") if down else
+            ("fp8 " + ("small_m" if M <= 64 else "large_m_pair")) if fp8 else
+            sg.swiglu_plan_string(M, K, N, variant))
     stream = torch.cuda.current_stream(dev)
 
     def fwd(j, s=None):
         """One forward on rotation slot j (on stream s, default the current stream)."""
-        if fp8:
+        if down:
+            sg.swiglu_down_forward(As[j], wps[j], K, R=Rs[j], Out=Ys[j], stream=s)
+        elif fp8:
             sg.swiglu_forward_fp8(As[j], wps[j], N, s_a, s_1, s_2, Y=Ys[j], stream=s)
         else:
             sg.swiglu_forward_variant(As[j], wps[j], N, variant, Y=Ys[j], stream=s)
@@ -293,7 +317,7 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     sg.swiglu_check_device_status(stream=stream)
     elapsed = t_begin.elapsed_time(t_end) * 1e-3
     elapsed_max = max_over_ranks(elapsed, world)
-    value = aggregate(w.flops, steps, elapsed_max, world)
+    value = aggregate(flops, steps, elapsed_max, world)
     # One fused-kernel launch per step and nothing else in the timed region, so
     # the average launch duration is the region's CUDA-event time over the
     # launches (events between launches would block the launch overlap).
@@ -305,7 +329,7 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     tensor_peak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
     tensor_sus = peaks.get("bf16_tflops_sustained")
     tensor_sus = tensor_sus * (2.0 if fp8 else 1.0) if tensor_sus else None
-    hbm_bound = w.flops / alg_bytes < tensor_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    hbm_bound = flops / alg_bytes < tensor_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
     kernel = ("fused_small_m_kernel" if plan.startswith("small_m") else
               "fused_large_m_pair_kernel" if plan.startswith("large_m_pair") else
               "fused_sequential_kernel" if plan.startswith("sequential") else
@@ -319,11 +343,11 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                 "traffic": traffic, "algorithmic_bytes": alg_bytes}
     else:
-        achieved = w.flops / avg_launch / 1e12
+        achieved = flops / avg_launch / 1e12
         sus = tensor_sus
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(tensor_peak, 1),
                 "unit": "TFLOP/s", "frac": round(achieved / tensor_peak, 4),
-                "traffic": traffic, "algorithmic_flops": w.flops,
+                "traffic": traffic, "algorithmic_flops": flops,
                 "peak_sustained": round(sus, 1) if sus else None,
                 "frac_sustained": round(achieved / sus, 4) if sus else None}
     roof.update({"kernel": kernel, "plan": plan, "avg_launch_us": round(avg_launch * 1e6, 3),
@@ -334,14 +358,20 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
 
     # ---- end to end through the public API: host activations in, host output out
     a_host = [a_cpu.pin_memory()] + [a_cpu.clone().pin_memory() for _ in range(min(copies, 4) - 1)]
-    y_host = [torch.empty(M, N, dtype=torch.bfloat16).pin_memory() for _ in range(len(a_host))]
-    a_dev = torch.empty(M, K, dtype=a_cpu.dtype, device=dev)
-    y_dev = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    y_host = [torch.empty(M, out_cols, dtype=torch.bfloat16).pin_memory()
+              for _ in range(len(a_host))]
+    a_dev = torch.empty(*a_cpu.shape, dtype=a_cpu.dtype, device=dev)
+    y_dev = torch.empty(M, out_cols, dtype=torch.bfloat16, device=dev)
     e2e_steps = steps
 
     def e2e_step(i):
         j = i % len(a_host)
-        if fp8:  # host copies through torch around the FP8 call
+        if down:  # host copies through torch around the down-projection call
+            a_dev.copy_(a_host[j], non_blocking=True)
+            sg.swiglu_down_forward(a_dev, wps[i % copies], K, R=Rs[i % copies], Out=y_dev,
+                                   stream=stream)
+            y_host[j].copy_(y_dev, non_blocking=True)
+        elif fp8:  # host copies through torch around the FP8 call
             a_dev.copy_(a_host[j], non_blocking=True)
             sg.swiglu_forward_fp8(a_dev, wps[i % copies], N, s_a, s_1, s_2, Y=y_dev, stream=stream)
             y_host[j].copy_(y_dev, non_blocking=True)
@@ -360,18 +390,20 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
     barrier(world)
     sg.swiglu_check_device_status(stream=stream)
-    e2e = {"value": round(aggregate(w.flops, e2e_steps, e2e_s, world), 3), "unit": "TFLOP/s",
-           "h2d_bytes_per_step": 2 * M * K, "d2h_bytes_per_step": 2 * M * N,
+    e2e = {"value": round(aggregate(flops, e2e_steps, e2e_s, world), 3), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": a_cpu.numel() * a_cpu.element_size(),
+           "d2h_bytes_per_step": 2 * M * out_cols,
            "steps": e2e_steps, "api": "swiglu_forward_from_host"}
 
     out = {
-        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "metric": METRIC_DOWN if down else METRIC, "value": round(value, 3), "unit": "TFLOP/s",
+        "n_gpus": world,
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(elapsed_max / steps * 1e3, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8-e4m3 (fp32 accumulate, bf16 out)" if fp8 else "bf16",
         "data": "synthetic",
         "config": {"workload": w.name, "M": M, "K": K, "N": N, "seed": w.seed,
-                   "variant": args.variant, "inputs": args.dtype,
+                   "variant": args.variant, "inputs": args.dtype, "op": args.op,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "launch": graph_note,
                    "l2": f"inputs larger than L2: {copies} rotating copies of A, packed W and Y "
@@ -581,6 +613,8 @@ def main(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--op", choices=["swiglu", "down"], default="swiglu",
+                   help="swiglu: the fused gate/up projection (default); down: Out = Y W3 + R")
     p.add_argument("--dtype", choices=["bf16", "fp8"], default="bf16",
                    help="input type: bf16 (the metric's), or E4M3 with per-tensor scales")
     p.add_argument("--variant", choices=sorted(VARIANTS), default="auto",

@@ -194,6 +194,30 @@ SWIGLU_API swiglu_status_t swiglu_forward_fp8(const void* A, const void* Wpacked
                                               swiglu_stream_t stream);
 
 /*
+ * The gated MLP's down-projection, the step after Y in the models the pages
+ * evaluate ("Tile-Level Activation Overlap for Efficient LLM Inference",
+ * gist.science, section "Problem Statement": the SwiGLU gated MLP; the pages
+ * do not describe this step further):
+ *   Out [M, H] = Y [M, N] x W3 [N, H] + R [M, H]     (bf16, fp32 accumulation)
+ * Y is the fused forward's output (N = the intermediate size), H the hidden
+ * size, R the block's residual input (NULL: none). Out may be R itself
+ * (in-place residual add); any other overlap is INVALID_ARG.
+ * Packed W3: tiles of 256 output columns x 64 K values, viewed as bf16
+ * [Hp/256][Np/64][256][64] with Wp[j][b][i][t] = W3[64b + t][256j + i], zero
+ * past the edges (Hp, Np = H, N rounded up to 256, 64); size
+ * swiglu_down_packed_bytes(N, H). M <= 64 (or M <= 128 with few 256-column
+ * output blocks) runs the decode kernel, with K split over clusters when H is
+ * narrow; larger M the CTA-pair kernel. N and H multiples of 8; errors as
+ * swiglu_forward.
+ */
+SWIGLU_API size_t swiglu_down_packed_bytes(int64_t N, int64_t H);
+SWIGLU_API swiglu_status_t swiglu_pack_down_weights(const void* W3, void* W3packed, int64_t N,
+                                                    int64_t H, swiglu_stream_t stream);
+SWIGLU_API swiglu_status_t swiglu_down_forward(const void* Y, const void* W3packed, const void* R,
+                                               void* Out, int64_t M, int64_t N, int64_t H,
+                                               swiglu_stream_t stream);
+
+/*
  * Allocation-free forward for callers that cannot call cudaMalloc: code that
  * runs while a stream is being captured into a CUDA graph (allocation is not
  * allowed there), serving runtimes that reserve all device memory for their

@@ -59,6 +59,12 @@ lib.swiglu_pack_weights_fp8.restype = _int
 lib.swiglu_forward_fp8.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_float, ctypes.c_float,
                                    ctypes.c_float, _vp]
 lib.swiglu_forward_fp8.restype = _int
+lib.swiglu_down_packed_bytes.argtypes = [_i64, _i64]
+lib.swiglu_down_packed_bytes.restype = _sz
+lib.swiglu_pack_down_weights.argtypes = [_vp, _vp, _i64, _i64, _vp]
+lib.swiglu_pack_down_weights.restype = _int
+lib.swiglu_down_forward.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]
+lib.swiglu_down_forward.restype = _int
 lib.swiglu_forward_noalloc.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp]
 lib.swiglu_forward_noalloc.restype = _int
 lib.swiglu_testing_inject_stall.argtypes = [_int, _u32]
@@ -228,6 +234,58 @@ def swiglu_forward_fp8(A: torch.Tensor, Wpacked: torch.Tensor, N: int, scale_a: 
                                       _stream_handle(stream, A.device)),
                "swiglu_forward_fp8")
     return Y
+
+
+def swiglu_down_packed_bytes(N: int, H: int) -> int:
+    return int(lib.swiglu_down_packed_bytes(int(N), int(H)))
+
+
+def swiglu_pack_down_weights(W3: torch.Tensor, W3packed: torch.Tensor | None = None,
+                             stream=None) -> torch.Tensor:
+    """Packed down-projection weight (flat bf16 buffer) from W3 [N, H] (bf16, CUDA)."""
+    _dev_bf16(W3, "W3")
+    if W3.dim() != 2:
+        raise ValueError("W3 must be [N, H]")
+    N, H = W3.shape
+    if W3packed is None:
+        W3packed = torch.empty(swiglu_down_packed_bytes(N, H) // 2, dtype=torch.bfloat16,
+                               device=W3.device)
+    _dev_bf16(W3packed, "W3packed")
+    if W3packed.numel() * 2 < swiglu_down_packed_bytes(N, H):
+        raise ValueError("W3packed is too small")
+    with _on_device(W3.device):
+        _check(lib.swiglu_pack_down_weights(W3.data_ptr(), W3packed.data_ptr(), N, H,
+                                            _stream_handle(stream, W3.device)),
+               "swiglu_pack_down_weights")
+    return W3packed
+
+
+def swiglu_down_forward(Y: torch.Tensor, W3packed: torch.Tensor, H: int,
+                        R: torch.Tensor | None = None, Out: torch.Tensor | None = None,
+                        stream=None) -> torch.Tensor:
+    """Out [M, H] = Y [M, N] x W3 + R (R optional; Out may be R for an in-place add)."""
+    _dev_bf16(Y, "Y")
+    _dev_bf16(W3packed, "W3packed")
+    if Y.dim() != 2:
+        raise ValueError("Y must be [M, N]")
+    M, N = Y.shape
+    if W3packed.numel() * 2 < swiglu_down_packed_bytes(N, H):
+        raise ValueError("W3packed does not hold a packed W3 for this N and H")
+    if R is not None:
+        _dev_bf16(R, "R")
+        if tuple(R.shape) != (M, H):
+            raise ValueError("R must be [M, H]")
+    if Out is None:
+        Out = torch.empty((M, H), dtype=torch.bfloat16, device=Y.device)
+    _dev_bf16(Out, "Out")
+    if tuple(Out.shape) != (M, H):
+        raise ValueError("Out must be [M, H]")
+    with _on_device(Y.device):
+        _check(lib.swiglu_down_forward(Y.data_ptr(), W3packed.data_ptr(),
+                                       R.data_ptr() if R is not None else None, Out.data_ptr(),
+                                       M, N, H, _stream_handle(stream, Y.device)),
+               "swiglu_down_forward")
+    return Out
 
 
 def swiglu_forward_from_host(A_host: torch.Tensor, Wpacked: torch.Tensor, N: int,

@@ -20,6 +20,11 @@
 //    completions arrive on both CTAs' "empty" and "accumulator full"
 //    barriers (multicast commit); both epilogues arrive on rank 0's
 //    "accumulator empty" barrier; every wait is bounded (ptx.cuh).
+//
+// With kDown the same pipeline computes the MLP's down-projection
+// Out = Y x W3 + R: a tile is 256 consecutive output columns (rank r loads
+// packed rows [128 r, 128 r + 128) of W3's tile), and the epilogue stores
+// accumulator + residual for all 256 columns.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -53,7 +58,7 @@ __device__ __forceinline__ void pair_tile_coords(int t, int tiles_m, int tiles_n
   nb = r / gm;
 }
 
-template <bool kFp8>
+template <bool kFp8, bool kDown>
 __global__ void __launch_bounds__(kThreads, 1)
     fused_large_m_pair_kernel(const __grid_constant__ LargeMParams p) {
   using C = PairCfg;
@@ -213,13 +218,71 @@ __global__ void __launch_bounds__(kThreads, 1)
       int mb, nb;
       pair_tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, mb, nb);
       const int row0 = mb * 2 * kTileM + static_cast<int>(rank) * kTileM + q * 32;
-      const int col0 = nb * C::kBN;
+      const int col0 = nb * (kDown ? 2 * C::kBN : C::kBN);
       int ok = 1;
       if (lane == 0) ok = mbar_wait(tfull0 + 8u * buf, acc_ph, wc, kSiteEpiTmemFull) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + lane_off + buf * C::kAccCols;
+      if constexpr (kDown) {
+        // 256 output columns: accumulator + residual, 32 columns per store
+        const __nv_bfloat16* res = reinterpret_cast<const __nv_bfloat16*>(p.residual);
+        const int row = row0 + lane;
+#pragma unroll 1
+        for (int c = 0; c < C::kAccCols / 32; ++c) {
+          uint32_t a[32];
+          tmem_ld_x32(tacc + c * 32, a);
+          tmem_wait_ld();
+          reg_fence(a);
+          if (c == C::kAccCols / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty0_lead + 8u * buf);
+          }
+          const int ncol = col0 + c * 32;
+          float add[32];
+#pragma unroll
+          for (int gq = 0; gq < 4; ++gq) {  // 8 columns (16 bytes) at a time; N % 8 == 0
+            const int col = ncol + gq * 8;
+            uint4 rv = make_uint4(0u, 0u, 0u, 0u);
+            if (res && row < p.M && col < p.N)
+              rv = *reinterpret_cast<const uint4*>(res + static_cast<size_t>(row) * p.N + col);
+            const uint32_t w4[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w4[e]);
+              add[gq * 8 + 2 * e] = __low2float(h);
+              add[gq * 8 + 2 * e + 1] = __high2float(h);
+            }
+          }
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+          const uint32_t stg = sStg + (ew * 2 + sbuf) * C::kStgBytes;
+          const uint32_t row_addr = stg + lane * 64;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int i0 = 8 * j + 2 * e;
+              w[e] = pack_bf16x2(__uint_as_float(a[i0]) + add[i0],
+                                 __uint_as_float(a[i0 + 1]) + add[i0 + 1]);
+            }
+            st_shared_v4(row_addr + ((j ^ ((lane >> 1) & 3)) << 4), w[0], w[1], w[2], w[3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (ncol < p.N && row0 < p.M) tma_store_2d(&p.tmap_y, stg, ncol, row0);
+            bulk_commit();
+          }
+          sbuf ^= 1;
+        }
+        buf ^= 1;
+        if (buf == 0) acc_ph ^= 1u;
+        continue;
+      }
 #pragma unroll 1
       for (int c = 0; c < C::kBN / 32; ++c) {
         uint32_t g[32], u[32];
@@ -296,18 +359,22 @@ cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribut
 }  // namespace
 
 cudaError_t configure_large_m_pair(int* max_pairs) {
-  cudaError_t e = cudaFuncSetAttribute(fused_large_m_pair_kernel<false>,
+  cudaError_t e = cudaFuncSetAttribute(fused_large_m_pair_kernel<false, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(PairCfg::kSmem));
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(fused_large_m_pair_kernel<true>,
+    e = cudaFuncSetAttribute(fused_large_m_pair_kernel<true, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(PairCfg::kSmem));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fused_large_m_pair_kernel<false, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(PairCfg::kSmem));
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pair_config(2, nullptr, attr, false);
   int clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&clusters, fused_large_m_pair_kernel<false>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&clusters, fused_large_m_pair_kernel<false, false>, &cfg);
   if (e != cudaSuccess) return e;
   *max_pairs = clusters;
   return cudaSuccess;
@@ -320,8 +387,11 @@ cudaError_t launch_large_m_pair(const LargeMParams& p, cudaStream_t stream) {
   if (p.grid < 2 || (p.grid % 2) != 0 || p.bn != PairCfg::kBN) return cudaErrorInvalidValue;
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pair_config(p.grid, stream, attr, pdl_enabled());
-  const cudaError_t e = p.fp8 ? cudaLaunchKernelEx(&cfg, fused_large_m_pair_kernel<true>, p)
-                              : cudaLaunchKernelEx(&cfg, fused_large_m_pair_kernel<false>, p);
+  if (p.fp8 && p.down) return cudaErrorInvalidValue;  // no FP8 down-projection
+  const cudaError_t e =
+      p.down ? cudaLaunchKernelEx(&cfg, fused_large_m_pair_kernel<false, true>, p)
+      : p.fp8 ? cudaLaunchKernelEx(&cfg, fused_large_m_pair_kernel<true, false>, p)
+              : cudaLaunchKernelEx(&cfg, fused_large_m_pair_kernel<false, false>, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

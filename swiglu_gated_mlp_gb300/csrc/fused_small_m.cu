@@ -21,6 +21,11 @@
 // a cluster barrier each CTA sums, through distributed shared memory, all
 // parts of its share of the block's columns, applies SiLU(g) * u and writes
 // those outputs. No global scratch is used.
+//
+// The same kernel computes the gated MLP's down-projection Out = Y x W3 + R
+// (kDown): a packed tile then holds 256 consecutive output columns, the two
+// accumulators are columns [0, 128) and [128, 256) of the block, and the
+// epilogue adds the residual instead of applying SiLU(g) * u.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -40,7 +45,7 @@ constexpr int kMaxStages = 8;
 constexpr size_t kSmemLimit = 232448;
 constexpr int kBarBytes = 256;
 
-template <bool kFp8>
+template <bool kFp8, bool kDown>
 __global__ void __launch_bounds__(kThreads, 1)
     fused_small_m_kernel(const __grid_constant__ SmallMParams p) {
   // K values per stage: 64 bf16 or 128 E4M3, a 128-byte row either way
@@ -200,6 +205,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           part_buf[(mt + mc * 16 + j) * kPackBlockN + r] = __uint_as_float(u[j]);
         }
       }
+    } else if (ok && kDown) {
+      // down-projection: thread r owns output columns n0 + r and n0 + 128 + r
+      tc_fence_after();
+      __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(p.y);
+      const __nv_bfloat16* res = reinterpret_cast<const __nv_bfloat16*>(p.residual);
+      const int n_lo = nblk * 2 * kPackBlockN + q * 32 + lane, n_hi = n_lo + kPackBlockN;
+#pragma unroll 1
+      for (int mc = 0; mc < mt / 16; ++mc) {
+        uint32_t g[16], u[16];
+        tmem_ld_x16(tmem_base + lane_off + mc * 16, g);
+        tmem_ld_x16(tmem_base + lane_off + mt + mc * 16, u);
+        tmem_wait_ld();
+        reg_fence(g);
+        reg_fence(u);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int m = mc * 16 + j;
+          if (m >= p.M) continue;
+          const size_t row = static_cast<size_t>(m) * p.N;
+          if (n_lo < p.N)
+            y[row + n_lo] = __float2bfloat16_rn(
+                __uint_as_float(g[j]) + (res ? __bfloat162float(res[row + n_lo]) : 0.0f));
+          if (n_hi < p.N)
+            y[row + n_hi] = __float2bfloat16_rn(
+                __uint_as_float(u[j]) + (res ? __bfloat162float(res[row + n_hi]) : 0.0f));
+        }
+      }
     } else if (ok) {
       tc_fence_after();
       __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(p.y);
@@ -246,6 +278,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         g.x += gs.x; g.y += gs.y; g.z += gs.z; g.w += gs.w;
         u.x += us.x; u.y += us.y; u.z += us.z; u.w += us.w;
       }
+      if constexpr (kDown) {  // columns n0 + r .. + 3 (g) and n0 + 128 + r .. + 3 (u)
+        const __nv_bfloat16* res = reinterpret_cast<const __nv_bfloat16*>(p.residual);
+        const int n_lo = nblk * 2 * kPackBlockN + r, n_hi = n_lo + kPackBlockN;
+        const size_t row = static_cast<size_t>(m) * p.N;
+        const float4 parts[2] = {g, u};
+        const int cols[2] = {n_lo, n_hi};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (cols[h] >= p.N) continue;  // N % 8 == 0: cols[h] < N implies cols[h] + 3 < N
+          float4 v = parts[h];
+          if (res) {
+            const uint2 rr = *reinterpret_cast<const uint2*>(res + row + cols[h]);
+            const __nv_bfloat162 r0 = *reinterpret_cast<const __nv_bfloat162*>(&rr.x);
+            const __nv_bfloat162 r1 = *reinterpret_cast<const __nv_bfloat162*>(&rr.y);
+            v.x += __low2float(r0); v.y += __high2float(r0);
+            v.z += __low2float(r1); v.w += __high2float(r1);
+          }
+          uint2 o;
+          o.x = pack_bf16x2(v.x, v.y);
+          o.y = pack_bf16x2(v.z, v.w);
+          *reinterpret_cast<uint2*>(y + row + cols[h]) = o;
+        }
+        continue;
+      }
       const int n = nblk * kPackBlockN + r;  // N % 8 == 0: n < N implies n + 3 < N
       if (kFp8) {
         g.x *= p.scale_gate; g.y *= p.scale_gate; g.z *= p.scale_gate; g.w *= p.scale_gate;
@@ -284,20 +340,22 @@ size_t small_m_smem_bytes(int mt, int stages) {
   return 1024 + size_t(stages) * (kWStageBytes + size_t(mt) * kBlockK * 2) + kBarBytes;
 }
 
-template <bool kFp8>
+template <bool kFp8, bool kDown>
 cudaError_t configure_small_m_t() {
-  cudaError_t e = cudaFuncSetAttribute(fused_small_m_kernel<kFp8>,
+  cudaError_t e = cudaFuncSetAttribute(fused_small_m_kernel<kFp8, kDown>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemLimit));
   if (e == cudaSuccess)  // all of the unified L1/shared array as shared memory (2 CTAs may share an SM)
-    e = cudaFuncSetAttribute(fused_small_m_kernel<kFp8>,
+    e = cudaFuncSetAttribute(fused_small_m_kernel<kFp8, kDown>,
                              cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   return e;
 }
 
 cudaError_t configure_small_m() {
-  const cudaError_t e = configure_small_m_t<false>();
-  return e != cudaSuccess ? e : configure_small_m_t<true>();
+  cudaError_t e = configure_small_m_t<false, false>();
+  if (e == cudaSuccess) e = configure_small_m_t<true, false>();
+  if (e == cudaSuccess) e = configure_small_m_t<false, true>();
+  return e;
 }
 
 cudaError_t static_scratch_address(uint32_t** out) {
@@ -323,7 +381,8 @@ int small_m_max_clusters(int splits) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, fused_small_m_kernel<false>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&clusters, fused_small_m_kernel<false, false>, &cfg) !=
+      cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -355,8 +414,11 @@ cudaError_t launch_small_m(const SmallMParams& p, cudaStream_t stream) {
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = splits > 1 ? 2 : 1;
-  const cudaError_t e = p.fp8 ? cudaLaunchKernelEx(&cfg, fused_small_m_kernel<true>, p)
-                              : cudaLaunchKernelEx(&cfg, fused_small_m_kernel<false>, p);
+  if (p.fp8 && p.down) return cudaErrorInvalidValue;  // no FP8 down-projection
+  const cudaError_t e =
+      p.down ? cudaLaunchKernelEx(&cfg, fused_small_m_kernel<false, true>, p)
+      : p.fp8 ? cudaLaunchKernelEx(&cfg, fused_small_m_kernel<true, false>, p)
+              : cudaLaunchKernelEx(&cfg, fused_small_m_kernel<false, false>, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -25,6 +25,8 @@ struct LargeMParams {
   int grid;  // persistent CTAs
   int fp8;   // E4M3 inputs (pair kernel): gate and up accumulators are scaled by
   float scale_gate, scale_up;  // scale_a * scale_w1 and scale_a * scale_w2 in the epilogue
+  int down;  // down-projection (pair kernel): tiles of 256 output columns, out = acc + residual
+  const void* residual;  // [M, N] bf16 or null (down-projection only)
   uint32_t* status;
   uint64_t timeout_ns;
   int inject_stall;
@@ -41,6 +43,9 @@ struct SmallMParams {
   int splits;  // K parts per column block (<= 1: none); > 1: clusters of `splits` CTAs
   int fp8;     // E4M3 inputs: accumulators are scaled by scale_gate / scale_up
   float scale_gate, scale_up;
+  int down;    // down-projection: a block is 256 output columns (rows 0-127 and 128-255
+               // of the packed tile), out = acc + residual instead of SiLU(g) * u
+  const void* residual;  // [M, N] bf16 or null (down-projection only)
   uint32_t* status;
   uint64_t timeout_ns;
   int inject_stall;
@@ -90,5 +95,7 @@ cudaError_t launch_pack(const void* w1, const void* w2, void* wp, int K, int N,
                         cudaStream_t stream);
 cudaError_t launch_pack_fp8(const void* w1, const void* w2, void* wp, int K, int N,
                             cudaStream_t stream);
+// Down-projection weight W3 [N, H] -> tiles of 256 output columns x 64 K values.
+cudaError_t launch_pack_down(const void* w3, void* wp, int N, int H, cudaStream_t stream);
 
 }  // namespace swg

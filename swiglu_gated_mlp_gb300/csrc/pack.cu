@@ -44,7 +44,38 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Down-projection weight W3 [N, H] (H contiguous) -> [Hp/256][Np/64][256][64]:
+// tile (j, b) row i is output column 256 j + i over K values 64 b .. 64 b + 63.
+__global__ void __launch_bounds__(256)
+    pack_down_kernel(const uint16_t* __restrict__ w3, uint16_t* __restrict__ wp, int N, int H,
+                     int k_slices) {
+  __shared__ uint16_t tile[kBlockK][kTileRows + 2];
+  const int b = blockIdx.x;  // K slice (rows of W3)
+  const int j = blockIdx.y;  // 256-column block of the output
+  const int k0 = b * kBlockK, h0 = j * kTileRows;
+  for (int idx = threadIdx.x; idx < kBlockK * kTileRows; idx += blockDim.x) {
+    const int t = idx / kTileRows, i = idx % kTileRows;
+    const int k = k0 + t, h = h0 + i;
+    tile[t][i] = (k < N && h < H) ? w3[static_cast<size_t>(k) * H + h] : uint16_t(0);
+  }
+  __syncthreads();
+  uint16_t* __restrict__ out =
+      wp + (static_cast<size_t>(j) * k_slices + b) * (static_cast<size_t>(kTileRows) * kBlockK);
+  for (int idx = threadIdx.x; idx < kBlockK * kTileRows; idx += blockDim.x) {
+    const int i = idx / kBlockK, t = idx % kBlockK;
+    out[idx] = tile[t][i];
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_pack_down(const void* w3, void* wp, int N, int H, cudaStream_t stream) {
+  const int blocks = (H + kTileRows - 1) / kTileRows;
+  const int k_slices = (N + kBlockK - 1) / kBlockK;
+  pack_down_kernel<<<dim3(k_slices, blocks), 256, 0, stream>>>(
+      static_cast<const uint16_t*>(w3), static_cast<uint16_t*>(wp), N, H, k_slices);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_pack(const void* w1, const void* w2, void* wp, int K, int N,
                         cudaStream_t stream) {

@@ -206,6 +206,18 @@ bool encode_packed_w(CUtensorMap* map, const void* base, int64_t K, int64_t N, u
   return encode_cached(map, base, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// The packed down-projection weight: {64 K values, 256 output columns, tiles}.
+int64_t padded_h(int64_t h) { return (h + 255) / 256 * 256; }
+
+bool encode_packed_down(CUtensorMap* map, const void* base, int64_t N, int64_t H, uint32_t rows) {
+  const int64_t tiles = (padded_h(H) / 256) * k_slices(N);
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(swg::kBlockK), 256,
+                              static_cast<cuuint64_t>(tiles)};
+  const cuuint64_t strides[2] = {swg::kBlockK * 2, 256u * swg::kBlockK * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(swg::kBlockK), rows, 1};
+  return encode_cached(map, base, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 // The FP8 packed weight: {128 one-byte K values, 256 rows, tiles}, 32 KB tiles.
 int64_t k_slices8(int64_t k) { return (k + swg::kBlockK8 - 1) / swg::kBlockK8; }
 
@@ -751,6 +763,119 @@ swiglu_status_t swiglu_forward_fp8(const void* A, const void* Wpacked, void* Y, 
     p.fp8 = 1;
     p.scale_gate = sg;
     p.scale_up = su;
+    p.status = d->status;
+    p.timeout_ns = g_timeout_ns.load();
+    p.inject_stall = g_inject.load();
+    err = swg::launch_large_m_pair(p, cs);
+  }
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_ERR_CUDA;
+  }
+  return SWIGLU_OK;
+}
+
+size_t swiglu_down_packed_bytes(int64_t N, int64_t H) {
+  if (N <= 0 || H <= 0 || N > kMaxKN || H > kMaxKN) return 0;
+  return size_t(padded_h(H)) * size_t(k_slices(N) * swg::kBlockK) * 2;
+}
+
+swiglu_status_t swiglu_pack_down_weights(const void* W3, void* W3packed, int64_t N, int64_t H,
+                                         swiglu_stream_t stream) {
+  swiglu_status_t st = check_shape(0, N, H);
+  if (st != SWIGLU_OK) return st;
+  if (!W3 || !W3packed) return SWIGLU_ERR_INVALID_ARG;
+  if (!aligned16(W3) || !aligned16(W3packed)) return SWIGLU_ERR_INVALID_ARG;
+  if (overlaps(W3packed, swiglu_down_packed_bytes(N, H), W3, size_t(N) * size_t(H) * 2))
+    return SWIGLU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != SWIGLU_OK) return st;
+  if (swg::launch_pack_down(W3, W3packed, static_cast<int>(N), static_cast<int>(H),
+                            reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_ERR_CUDA;
+  }
+  return SWIGLU_OK;
+}
+
+swiglu_status_t swiglu_down_forward(const void* Y, const void* W3packed, const void* R, void* Out,
+                                    int64_t M, int64_t N, int64_t H, swiglu_stream_t stream) {
+  swiglu_status_t st = check_shape(M, N, H);
+  if (st != SWIGLU_OK) return st;
+  if (M == 0) return SWIGLU_OK;
+  if (!Y || !W3packed || !Out) return SWIGLU_ERR_INVALID_ARG;
+  if (!aligned16(Y) || !aligned16(W3packed) || !aligned16(Out) || (R && !aligned16(R)))
+    return SWIGLU_ERR_INVALID_ARG;
+  const size_t y_bytes = size_t(M) * size_t(N) * 2, o_bytes = size_t(M) * size_t(H) * 2;
+  if (overlaps(Out, o_bytes, Y, y_bytes) ||
+      overlaps(Out, o_bytes, W3packed, swiglu_down_packed_bytes(N, H)) ||
+      (R && R != Out && overlaps(Out, o_bytes, R, o_bytes)))  // Out == R (in place) is allowed
+    return SWIGLU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != SWIGLU_OK) return st;
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t blocks = padded_h(H) / 256;  // 256 output columns per block
+  const int64_t ks = k_slices(N);
+  cudaError_t err;
+  // decode kernel for few tokens, or up to 128 tokens when there are few output
+  // blocks for the SMs (K then splits over clusters); CTA pairs otherwise
+  if (M <= 64 || (M <= swg::kTileM && blocks * 2 <= d->sm_count)) {
+    // decode: weights as the MMA M side, K split over clusters when blocks are few
+    swg::SmallMParams p{};
+    p.mt = static_cast<int>((M + 15) / 16 * 16);
+    p.stages = swg::small_m_stages(p.mt, 1);
+    if (blocks > d->sm_count && swg::small_m_stages(p.mt, 2) >= 3)
+      p.stages = swg::small_m_stages(p.mt, 2);
+    p.splits = 1;
+    const int64_t stage_bytes = 2 * swg::kPackBlockN * swg::kBlockK * 2 + int64_t(p.mt) * 128;
+    if (p.mt <= 128 && int64_t(p.mt) * 1024 <= p.stages * stage_bytes) {
+      for (int s : {8, 4, 2}) {
+        if (blocks * s <= d->sm_count && s <= ks && d->small_clusters[s] >= blocks) {
+          p.splits = s;
+          break;
+        }
+      }
+    }
+    if (!encode_2d(&p.tmap_x, Y, N, M, N * 2, swg::kBlockK, p.mt, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_packed_down(&p.tmap_w, W3packed, N, H, 256))
+      return SWIGLU_ERR_CUDA;
+    p.y = Out;
+    p.residual = R;
+    p.down = 1;
+    p.M = static_cast<int>(M);
+    p.K = static_cast<int>(N);
+    p.N = static_cast<int>(H);
+    p.grid = static_cast<int>(blocks * p.splits);
+    p.status = d->status;
+    p.timeout_ns = g_timeout_ns.load();
+    p.inject_stall = g_inject.load();
+    err = swg::launch_small_m(p, cs);
+  } else {
+    if (d->max_pairs < 1) return SWIGLU_ERR_UNSUPPORTED;
+    swg::LargeMParams p{};
+    const int64_t pm = (M + 2 * swg::kTileM - 1) / (2 * swg::kTileM);
+    const int64_t tiles = pm * blocks;
+    if (tiles > 2147483647) return SWIGLU_ERR_UNSUPPORTED;
+    int64_t group = (48ll << 20) / (int64_t(2 * swg::kTileM) * N * 2);
+    if (group < 1) group = 1;
+    if (group > pm) group = pm;
+    if (!encode_2d(&p.tmap_a, Y, N, M, N * 2, swg::kBlockK, swg::kTileM,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_packed_down(&p.tmap_w, W3packed, N, H, swg::kPackBlockN) ||
+        !encode_2d(&p.tmap_y, Out, H, M, H * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+      return SWIGLU_ERR_CUDA;
+    p.M = static_cast<int>(M);
+    p.K = static_cast<int>(N);
+    p.N = static_cast<int>(H);
+    p.tiles_m = static_cast<int>(pm);
+    p.tiles_n = static_cast<int>(blocks);
+    p.group_m = static_cast<int>(group);
+    p.bn = swg::kPackBlockN;
+    p.grid = 2 * static_cast<int>(tiles < d->max_pairs ? tiles : d->max_pairs);
+    p.down = 1;
+    p.residual = R;
     p.status = d->status;
     p.timeout_ns = g_timeout_ns.load();
     p.inject_stall = g_inject.load();

@@ -363,3 +363,42 @@ def test_fp8_pack_layout_uses_128_value_slices():
             b, t = divmod(k, 128)
             assert p[j, b, i, t] == w1[k, n] and p[j, b, 128 + i, t] == w2[k, n]
     assert not p[1, :, 8:128].any() and not p[:, 1, :, 72:].any()
+
+
+# ----------------------------------------------------- down-projection ----
+
+def test_down_reference_matches_brute_force():
+    from oracle.down_ref import down_f64
+    import math as _m
+    y, w3, _ = make_inputs(5, 24, 9, seed=31)          # Y [5, 24], W3 [24, 9]
+    r, _, _ = make_inputs(5, 9, 1, seed=32)            # R [5, 9]
+    yb, w3b, rb = bf16_bits(y), bf16_bits(w3), bf16_bits(r)
+    yv, w3v, rv = (bf16_bits_to_f64(x) for x in (yb, w3b, rb))
+    want = np.array([[_m.fsum([*(yv[m, k] * w3v[k, h] for k in range(24)), rv[m, h]])
+                      for h in range(9)] for m in range(5)])
+    assert np.allclose(down_f64(yb, w3b, rb), want, rtol=1e-14, atol=1e-15)
+    assert np.allclose(down_f64(yb, w3b, None), want - rv, rtol=1e-13, atol=1e-14)
+
+
+def test_down_reference_identity_and_rows():
+    from oracle.down_ref import down_f64_values, down_f64
+    y = np.array([[1.0, -2.0, 0.5]])
+    assert np.array_equal(down_f64_values(y, np.eye(3), np.array([[1.0, 1.0, 1.0]])),
+                          [[2.0, -1.0, 1.5]])
+    yv, w3, _ = make_inputs(7, 16, 5, seed=33)
+    full = down_f64(bf16_bits(yv), bf16_bits(w3))
+    assert np.array_equal(down_f64(bf16_bits(yv), bf16_bits(w3), rows=[6, 1]), full[[6, 1]])
+
+
+def test_down_pack_layout():
+    from oracle.down_ref import pack_down_reference
+    rng = np.random.default_rng(8)
+    w3 = rng.integers(0, 2 ** 16, size=(100, 300), dtype=np.uint16)   # N=100, H=300
+    p = pack_down_reference(w3)
+    assert p.shape == (2, 2, 256, 64)
+    for h in (0, 255, 256, 299):
+        j, i = divmod(h, 256)
+        for k in (0, 63, 64, 99):
+            b, t = divmod(k, 64)
+            assert p[j, b, i, t] == w3[k, h]
+    assert not p[1, :, 44:].any() and not p[:, 1, :, 36:].any()
