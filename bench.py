@@ -259,7 +259,8 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     down_small = M <= 64 or (M <= 128 and 2 * (-(-K // 256)) <= sms)
     plan = (("down small_m" if down_small else "down large_m_pair") if down else
-            ("fp8 " + ("small_m" if M <= 64 else "large_m_pair")) if fp8 else
+            ("fp8 " + ("small_m" if (M <= 32 or (M <= 64 and 2 * (-(-N // 128)) <= sms))
+                       else "large_m_pair")) if fp8 else
             sg.swiglu_plan_string(M, K, N, variant))
     stream = torch.cuda.current_stream(dev)
 

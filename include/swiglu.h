@@ -181,8 +181,8 @@ SWIGLU_API swiglu_status_t swiglu_plan_string(int64_t M, int64_t K, int64_t N, i
  * viewed as bytes [Np/128][Kp/128][256][128], Kp = K rounded up to 128; size
  * 2 * Np * Kp bytes. swiglu_pack_weights_fp8 takes W1_8, W2_8 as [K, N]
  * E4M3 row-major device arrays. swiglu_forward_fp8 takes A8 [M, K] E4M3 and
- * writes Y [M, N] bf16; M <= 64 uses the decode kernel, larger M the CTA-pair
- * kernel. Requirements and errors as the bf16 calls, plus K a multiple of 16
+ * writes Y [M, N] bf16; M <= 32 (or <= 64 on narrow N) uses the decode
+ * kernel, larger M the CTA-pair kernel. Requirements and errors as the bf16 calls, plus K a multiple of 16
  * (UNSUPPORTED) and finite scales (INVALID_ARG).
  */
 SWIGLU_API size_t swiglu_packed_weight_bytes_fp8(int64_t K, int64_t N);

@@ -73,8 +73,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int num_kb = (p.K + kBK - 1) / kBK;
   const int splits = p.splits > 1 ? p.splits : 1;
-  const int nblk = blockIdx.x / splits;
+  // CTA index = ((column block * token groups) + token group) * splits + K part
+  const int mgroups = p.mgroups > 1 ? p.mgroups : 1;
   const int part = blockIdx.x % splits;  // the CTA's rank in its cluster when splits > 1
+  const int tgroup = (blockIdx.x / splits) % mgroups;
+  const int nblk = blockIdx.x / (splits * mgroups);
+  const int m0 = tgroup * mt;                 // first token of this CTA's group
+  const int mcount = min(mt, p.M - m0);       // tokens in the group
   const int kb_begin = part * num_kb / splits;
   const int kb_end = (part + 1) * num_kb / splits;
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
@@ -121,7 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int k0 = kb * kBK;
           mbar_arrive_expect_tx(fb, stage_bytes);
           tma_load_3d_hint(sw, &p.tmap_w, fb, 0, 0, wtile + kb, pol_w);  // one contiguous 32 KB tile
-          tma_load_2d_hint(sw + kWStageBytes, &p.tmap_x, fb, k0, 0, pol_x);
+          tma_load_2d_hint(sw + kWStageBytes, &p.tmap_x, fb, k0, m0, pol_x);
           filled |= 1u << s;
           fill_ph = (fill_ph & ~(1u << s)) | (ph << s);
         }
@@ -222,8 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int m = mc * 16 + j;
-          if (m >= p.M) continue;
-          const size_t row = static_cast<size_t>(m) * p.N;
+          if (m >= mcount) continue;
+          const size_t row = static_cast<size_t>(m0 + m) * p.N;
           if (n_lo < p.N)
             y[row + n_lo] = __float2bfloat16_rn(
                 __uint_as_float(g[j]) + (res ? __bfloat162float(res[row + n_lo]) : 0.0f));
@@ -248,8 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int m = mc * 16 + j;
-            if (m < p.M)
-              y[static_cast<size_t>(m) * p.N + n] = __float2bfloat16_rn(
+            if (m < mcount)
+              y[static_cast<size_t>(m0 + m) * p.N + n] = __float2bfloat16_rn(
                   silu_mul(sg * __uint_as_float(g[j]), su * __uint_as_float(u[j])));
           }
         }
@@ -266,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int chunks = rows / 4;
     const uint32_t local = smem_addr(smem);
     __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(p.y);
-    for (int idx = threadIdx.x; idx < p.M * chunks; idx += blockDim.x) {
+    for (int idx = threadIdx.x; idx < mcount * chunks; idx += blockDim.x) {
       const int m = idx / chunks;
       const int r = part * rows + (idx % chunks) * 4;
       float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
@@ -281,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (kDown) {  // columns n0 + r .. + 3 (g) and n0 + 128 + r .. + 3 (u)
         const __nv_bfloat16* res = reinterpret_cast<const __nv_bfloat16*>(p.residual);
         const int n_lo = nblk * 2 * kPackBlockN + r, n_hi = n_lo + kPackBlockN;
-        const size_t row = static_cast<size_t>(m) * p.N;
+        const size_t row = static_cast<size_t>(m0 + m) * p.N;
         const float4 parts[2] = {g, u};
         const int cols[2] = {n_lo, n_hi};
 #pragma unroll
@@ -311,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint2 v;
         v.x = pack_bf16x2(silu_mul(g.x, u.x), silu_mul(g.y, u.y));
         v.y = pack_bf16x2(silu_mul(g.z, u.z), silu_mul(g.w, u.w));
-        *reinterpret_cast<uint2*>(y + static_cast<size_t>(m) * p.N + n) = v;
+        *reinterpret_cast<uint2*>(y + static_cast<size_t>(m0 + m) * p.N + n) = v;
       }
     }
     cluster_sync();  // no CTA leaves while a peer may still read its partials

@@ -41,6 +41,7 @@ struct SmallMParams {
   int stages;  // pipeline depth
   int grid;    // one CTA per 128-column block and K part (splits)
   int splits;  // K parts per column block (<= 1: none); > 1: clusters of `splits` CTAs
+  int mgroups; // token groups of mt rows each (<= 1: one group holds all M tokens)
   int fp8;     // E4M3 inputs: accumulators are scaled by scale_gate / scale_up
   float scale_gate, scale_up;
   int down;    // down-projection: a block is 256 output columns (rows 0-127 and 128-255

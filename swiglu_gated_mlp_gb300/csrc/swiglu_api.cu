@@ -235,7 +235,39 @@ struct Plan {
   int variant = SWIGLU_VARIANT_AUTO;
   int bn = 0, stages = 0, tiles_m = 0, tiles_n = 0, group_m = 0, tiles = 0, grid = 0, mt = 0;
   int splits = 1;
+  int mgroups = 1;
 };
+
+// Decode-kernel work split for `blocks` weight blocks and M tokens: token
+// groups of mt rows, pipeline depth, and K parts per cluster. With few blocks
+// for the SMs, more than 64 tokens go in 64-token groups (each group streams
+// the same weights, the repeats coming from L2), and each (block, group) unit
+// splits K over a cluster so that the units fill the SMs; all clusters must be
+// resident at once.
+void decode_split_plan(int64_t M, int64_t blocks, int64_t kslices, const DeviceState* d,
+                       int* mt, int* mgroups, int* stages, int* splits) {
+  const int sm_count = d ? d->sm_count : 0;
+  *mt = static_cast<int>((M + 15) / 16 * 16);
+  *mgroups = 1;
+  if (d && M > 64 && blocks * 2 <= sm_count) {
+    *mt = 64;
+    *mgroups = static_cast<int>((M + 63) / 64);
+  }
+  const int64_t units = blocks * *mgroups;
+  *stages = swg::small_m_stages(*mt, 1);
+  if (sm_count > 0 && units > sm_count && swg::small_m_stages(*mt, 2) >= 3)
+    *stages = swg::small_m_stages(*mt, 2);
+  *splits = 1;
+  const int64_t stage_bytes = 2 * swg::kPackBlockN * swg::kBlockK * 2 + int64_t(*mt) * 128;
+  if (d && *mt <= 128 && int64_t(*mt) * 1024 <= *stages * stage_bytes) {
+    for (int s : {8, 4, 2}) {
+      if (units * s <= sm_count && s <= kslices && d->small_clusters[s] >= units) {
+        *splits = s;
+        break;
+      }
+    }
+  }
+}
 
 // `d` may be null (allocation-free entry point): no SM count, no cluster data.
 swiglu_status_t make_plan(int64_t M, int64_t K, int64_t N, int variant, const DeviceState* d,
@@ -263,28 +295,12 @@ swiglu_status_t make_plan(int64_t M, int64_t K, int64_t N, int variant, const De
   pl->variant = variant;
   if (variant == SWIGLU_VARIANT_SMALL_M) {
     if (M > 256) return SWIGLU_ERR_UNSUPPORTED;
-    pl->mt = static_cast<int>((M + 15) / 16 * 16);
     pl->tiles = static_cast<int>(np / swg::kPackBlockN);
-    // One CTA per SM with the deepest ring, unless there are more column blocks
-    // than SMs: then two CTAs per SM (3+ stages each) keep the whole grid
-    // resident instead of running a second, partial wave.
-    pl->stages = swg::small_m_stages(pl->mt, 1);
-    if (sm_count > 0 && pl->tiles > sm_count && swg::small_m_stages(pl->mt, 2) >= 3)
-      pl->stages = swg::small_m_stages(pl->mt, 2);
-    // Few column blocks for the SMs: split each block's K range over a cluster
-    // of CTAs (largest split that keeps every cluster resident at once).
-    pl->splits = 1;
-    const int64_t stage_bytes = 2 * swg::kPackBlockN * swg::kBlockK * 2 + int64_t(pl->mt) * swg::kBlockK * 2;
-    // (only for few tokens: with more, the partials' exchange costs more than it saves)
-    if (d && pl->mt <= 64 && int64_t(pl->mt) * 1024 <= pl->stages * stage_bytes) {
-      for (int s : {8, 4, 2}) {
-        if (pl->tiles * s <= sm_count && s <= kslices && d->small_clusters[s] >= pl->tiles) {
-          pl->splits = s;
-          break;
-        }
-      }
-    }
-    pl->grid = pl->tiles * pl->splits;
+    // One CTA per SM with the deepest ring, unless there are more (block, token
+    // group) units than SMs: then two CTAs per SM (3+ stages each) keep the
+    // whole grid resident; with few units, K splits over clusters.
+    decode_split_plan(M, pl->tiles, kslices, d, &pl->mt, &pl->mgroups, &pl->stages, &pl->splits);
+    pl->grid = pl->tiles * pl->mgroups * pl->splits;
     return SWIGLU_OK;
   }
   if (variant == SWIGLU_VARIANT_SEQUENTIAL) {
@@ -386,6 +402,7 @@ swiglu_status_t launch_forward(const void* A, const void* Wp, void* Y, int64_t M
     p.stages = pl.stages;
     p.grid = pl.grid;
     p.splits = pl.splits;
+    p.mgroups = pl.mgroups;
     p.status = d.status;
     p.timeout_ns = timeout;
     p.inject_stall = inject;
@@ -607,8 +624,9 @@ swiglu_status_t swiglu_plan_string(int64_t M, int64_t K, int64_t N, int variant,
   st = make_plan(M < 1 ? 1 : M, K, N, variant, d, &pl);
   if (st != SWIGLU_OK) return st;
   if (pl.variant == SWIGLU_VARIANT_SMALL_M)
-    std::snprintf(buf, buflen, "small_m mt=%d stages=%d tiles=%d splits=%d grid=%d sms=%d", pl.mt,
-                  pl.stages, pl.tiles, pl.splits, pl.grid, d->sm_count);
+    std::snprintf(buf, buflen,
+                  "small_m mt=%d stages=%d tiles=%d groups=%d splits=%d grid=%d sms=%d", pl.mt,
+                  pl.stages, pl.tiles, pl.mgroups, pl.splits, pl.grid, d->sm_count);
   else if (pl.variant == SWIGLU_VARIANT_SEQUENTIAL)
     std::snprintf(buf, buflen, "sequential bn=%d stages=%d tiles=%d grid=%d group_m=%d sms=%d",
                   pl.bn, pl.stages, pl.tiles, pl.grid, pl.group_m, d->sm_count);
@@ -716,9 +734,11 @@ swiglu_status_t swiglu_forward_fp8(const void* A, const void* Wpacked, void* Y, 
   DeviceState* d = nullptr;
   st = device_state(&d);
   if (st != SWIGLU_OK) return st;
-  // Decode sizes take the decode kernel, the rest CTA pairs (the two FP8 kernels).
+  // As for bf16: the decode kernel for up to 32 tokens, or up to 64 on narrow N;
+  // CTA pairs otherwise (the two FP8 kernels).
   Plan pl;
-  const bool small = M <= 64;
+  const int64_t nb = padded_n(N) / swg::kPackBlockN;
+  const bool small = M <= 32 || (M <= 64 && nb * 2 <= d->sm_count) || d->max_pairs < 1;
   st = make_plan(M, K, N, small ? SWIGLU_VARIANT_SMALL_M : SWIGLU_VARIANT_LARGE_M_PAIR, d, &pl, 1);
   if (st != SWIGLU_OK) return st;
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
@@ -738,6 +758,7 @@ swiglu_status_t swiglu_forward_fp8(const void* A, const void* Wpacked, void* Y, 
     p.stages = pl.stages;
     p.grid = pl.grid;
     p.splits = pl.splits;
+    p.mgroups = pl.mgroups;
     p.fp8 = 1;
     p.scale_gate = sg;
     p.scale_up = su;
@@ -824,20 +845,7 @@ swiglu_status_t swiglu_down_forward(const void* Y, const void* W3packed, const v
   if (M <= 64 || (M <= swg::kTileM && blocks * 2 <= d->sm_count)) {
     // decode: weights as the MMA M side, K split over clusters when blocks are few
     swg::SmallMParams p{};
-    p.mt = static_cast<int>((M + 15) / 16 * 16);
-    p.stages = swg::small_m_stages(p.mt, 1);
-    if (blocks > d->sm_count && swg::small_m_stages(p.mt, 2) >= 3)
-      p.stages = swg::small_m_stages(p.mt, 2);
-    p.splits = 1;
-    const int64_t stage_bytes = 2 * swg::kPackBlockN * swg::kBlockK * 2 + int64_t(p.mt) * 128;
-    if (p.mt <= 128 && int64_t(p.mt) * 1024 <= p.stages * stage_bytes) {
-      for (int s : {8, 4, 2}) {
-        if (blocks * s <= d->sm_count && s <= ks && d->small_clusters[s] >= blocks) {
-          p.splits = s;
-          break;
-        }
-      }
-    }
+    decode_split_plan(M, blocks, ks, d, &p.mt, &p.mgroups, &p.stages, &p.splits);
     if (!encode_2d(&p.tmap_x, Y, N, M, N * 2, swg::kBlockK, p.mt, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_packed_down(&p.tmap_w, W3packed, N, H, 256))
       return SWIGLU_ERR_CUDA;
@@ -847,7 +855,7 @@ swiglu_status_t swiglu_down_forward(const void* Y, const void* W3packed, const v
     p.M = static_cast<int>(M);
     p.K = static_cast<int>(N);
     p.N = static_cast<int>(H);
-    p.grid = static_cast<int>(blocks * p.splits);
+    p.grid = static_cast<int>(blocks * p.mgroups * p.splits);
     p.status = d->status;
     p.timeout_ns = g_timeout_ns.load();
     p.inject_stall = g_inject.load();

@@ -71,6 +71,19 @@ def test_small_m_split_k_matches_oracle(native, M, K, N):
     check_against_oracle(native, M, K, N, seed=M * 11 + K + N, variant=SMALL)
 
 
+# More than 64 tokens on few column blocks: 64-token groups, each group's K
+# range split over a cluster.
+GROUP_CASES = [(128, 896, 4864), (65, 256, 256), (100, 1000, 1032), (200, 512, 1000),
+               (256, 384, 264)]
+
+
+@pytest.mark.parametrize("M,K,N", GROUP_CASES)
+def test_small_m_token_groups_match_oracle(native, M, K, N):
+    plan = native.swiglu_plan_string(M, K, N, SMALL)
+    assert "groups=1 " not in plan, plan
+    check_against_oracle(native, M, K, N, seed=M * 17 + K + N, variant=SMALL)
+
+
 @pytest.mark.parametrize("M,K,N", SMALL_CASES)
 def test_small_m_kernel_matches_oracle(native, M, K, N):
     check_against_oracle(native, M, K, N, seed=M * 7 + K + N, variant=SMALL)
