@@ -54,7 +54,7 @@ def test_fp8_pack_is_bit_exact(native, K, N):
 CASES = [
     (1, 128, 128), (16, 3584, 1280), (16, 144, 136), (33, 400, 264), (64, 896, 4864),
     (16, 896, 4864), (65, 256, 512), (100, 400, 264), (256, 1024, 1024), (300, 512, 1000),
-    (1000, 2048, 768),
+    (1000, 2048, 768), (48, 512, 20480),
 ]
 
 
