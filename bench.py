@@ -407,9 +407,11 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
                    "variant": args.variant, "inputs": args.dtype, "op": args.op,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "launch": graph_note,
-                   "l2": f"inputs larger than L2: {copies} rotating copies of A, packed W and Y "
+                   "l2": f"inputs larger than L2: {copies} rotating copies of "
+                         f"{'Y, packed W3, R and Out' if down else 'A, packed W and Y'} "
                          f"({copies * alg_bytes / 2**20:.0f} MiB)",
-                   "note": w.note},
+                   "note": (f"down-projection Out[M,H] = Y[M,N] W3[N,H] + R at this workload's "
+                            f"MLP shape, H = {K}" if down else w.note)},
         "pct_bf16_peak": round(100 * value / world / peaks["bf16_tflops"], 3),
         "pct_of_dtype_peak": round(100 * value / world / tensor_peak, 3),
         "roofline": roof,
