@@ -245,7 +245,14 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     w_bytes = wp0.numel() * wp0.element_size()
     # Inputs larger than L2 between consecutive steps: rotate copies of the
     # packed weight (and of A and Y) so no step finds its operands in L2.
-    copies = max(2, math.ceil(3 * L2_BYTES / max(alg_bytes, 1)))
+    # Between two uses of one copy the other copies stream at least 32 x L2
+    # bytes: the decode kernel stages weight tiles in L2 ahead of its pipeline,
+    # and those lines were measured to outlive several x L2 of evict-first
+    # streaming, so a shallow rotation would let a step find some of its
+    # weights still cached from the previous use of the same copy.
+    copies = 1 + max(1, math.ceil(32 * L2_BYTES / max(alg_bytes, 1)))
+    if args.rotate:
+        copies = max(2, args.rotate)
     copies = min(copies, 64)
     wps = [wp0] + [wp0.clone() for _ in range(copies - 1)]
     a0 = a_cpu.to(dev)
@@ -409,7 +416,9 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
                    "launch": graph_note,
                    "l2": f"inputs larger than L2: {copies} rotating copies of "
                          f"{'Y, packed W3, R and Out' if down else 'A, packed W and Y'} "
-                         f"({copies * alg_bytes / 2**20:.0f} MiB)",
+                         f"({copies * alg_bytes / 2**20:.0f} MiB; "
+                         f"{(copies - 1) * alg_bytes / 2**20:.0f} MiB of other copies "
+                         f"between two uses of one)",
                    "note": (f"down-projection Out[M,H] = Y[M,N] W3[N,H] + R at this workload's "
                             f"MLP shape, H = {K}" if down else w.note)},
         "pct_bf16_peak": round(100 * value / world / peaks["bf16_tflops"], 3),
@@ -615,6 +624,9 @@ def main(argv=None):
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--rotate", type=int, default=0,
+                   help="rotating copies of the operands (0: enough that 32 x L2 bytes of "
+                        "other copies are read between two uses of one)")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--op", choices=["swiglu", "down"], default="swiglu",
                    help="swiglu: the fused gate/up projection (default); down: Out = Y W3 + R")

@@ -87,6 +87,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     prefetch_tmap(&p.tmap_x);
     prefetch_tmap(&p.tmap_w);
+    // The packed weight is an input of the decode step, not a product of the
+    // kernel before it in the stream; fetching this CTA's first tiles into L2
+    // before the grid-dependency wait overlaps their DRAM latency with the
+    // previous grid's tail. L2 is coherent, so this is safe even when that
+    // kernel did write the weight: the loads after the wait see its writes.
+    const int npre = min(p.l2_prefetch, kb_end - kb_begin);
+    const uint64_t pol = policy_evict_first();
+    for (int i = 0; i < npre; ++i)
+      tma_prefetch_l2_3d_hint(&p.tmap_w, 0, 0, nblk * num_kb + kb_begin + i, pol);
     for (int s = 0; s < stages; ++s) {
       mbar_init(full0 + 8u * s, 1);
       mbar_init(empty0 + 8u * s, 1);
@@ -405,6 +414,8 @@ cudaError_t launch_small_m(const SmallMParams& p, cudaStream_t stream) {
        size_t(2) * p.mt * kPackBlockN * 4 > size_t(p.stages) * (kWStageBytes + size_t(p.mt) * kBlockK * 2) ||
        (p.grid % splits) != 0))
     return cudaErrorInvalidValue;
+  SmallMParams q = p;
+  q.l2_prefetch = small_m_l2_prefetch(p.grid, p.splits);
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(p.grid);
   cfg.blockDim = dim3(kThreads);
@@ -421,9 +432,9 @@ cudaError_t launch_small_m(const SmallMParams& p, cudaStream_t stream) {
   cfg.numAttrs = splits > 1 ? 2 : 1;
   if (p.fp8 && p.down) return cudaErrorInvalidValue;  // no FP8 down-projection
   const cudaError_t e =
-      p.down ? cudaLaunchKernelEx(&cfg, fused_small_m_kernel<false, true>, p)
-      : p.fp8 ? cudaLaunchKernelEx(&cfg, fused_small_m_kernel<true, false>, p)
-              : cudaLaunchKernelEx(&cfg, fused_small_m_kernel<false, false>, p);
+      p.down ? cudaLaunchKernelEx(&cfg, fused_small_m_kernel<false, true>, q)
+      : p.fp8 ? cudaLaunchKernelEx(&cfg, fused_small_m_kernel<true, false>, q)
+              : cudaLaunchKernelEx(&cfg, fused_small_m_kernel<false, false>, q);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -50,6 +50,7 @@ struct SmallMParams {
   uint32_t* status;
   uint64_t timeout_ns;
   int inject_stall;
+  int l2_prefetch;  // packed tiles per CTA staged in L2 before the grid-dependency wait
 };
 
 // One-time per-device set-up (dynamic shared-memory limits of every instantiation).
@@ -86,6 +87,9 @@ int small_m_stages(int mt, int ctas_per_sm);
 // environment sets SWIGLU_PDL=0): a launch may begin while the previous grid
 // in the stream drains; the kernel waits for it before touching memory.
 bool pdl_enabled();
+// Packed weight tiles each decode CTA stages in L2 ahead of its pipeline, for
+// a grid of `grid` CTAs in clusters of `splits` (SWIGLU_L2_PREFETCH=n forces n).
+int small_m_l2_prefetch(int grid, int splits);
 size_t small_m_smem_bytes(int mt, int stages);
 cudaError_t launch_small_m(const SmallMParams& p, cudaStream_t stream);
 // Clusters of `splits` decode CTAs (shared memory at the 1-CTA-per-SM limit)

@@ -147,6 +147,19 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
+// Bring one 3-D tile of a tensor from global memory into L2 (no shared-memory
+// destination, no barrier) under an L2 eviction policy. L2 is the point of
+// coherence, so a line fetched here never hides a later write by another kernel
+// from a load that follows.
+__device__ __forceinline__ void tma_prefetch_l2_3d_hint(const CUtensorMap* map, int32_t c0,
+                                                        int32_t c1, int32_t c2, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.3d.L2.global.tile.L2::cache_hint [%0, {%1, %2, %3}], %4;" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+      : "memory");
+}
+
 // 2-D tiled load global -> shared; completion counted in bytes on `bar`.
 // c0 is the innermost (contiguous) coordinate; it is always a multiple of 64
 // elements here (128 bytes), so the 16-byte rule for TMA holds.

@@ -2,6 +2,7 @@
 // kernel choice and launch. Declarations and contracts are in include/swiglu.h.
 #include "swiglu.h"
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdio>
@@ -54,6 +55,18 @@ namespace swg {
 bool pdl_enabled() {
   static const bool on = env_int("SWIGLU_PDL", 1) != 0;
   return on;
+}
+// Decode-kernel L2 staging depth. About 64 MB over the whole grid: deeper
+// staging measured slower (the staged lines start to displace one another).
+// K-split clusters stage 4 tiles: their grids leave SMs idle, so the next grid
+// starts early and deep staging competes with the current grid's tail.
+int small_m_l2_prefetch(int grid, int splits) {
+  static const int64_t forced = env_int("SWIGLU_L2_PREFETCH", -1);
+  if (forced >= 0) return static_cast<int>(std::min<int64_t>(forced, 64));
+  if (splits > 1) return 4;
+  const int64_t budget = int64_t(64) << 20;
+  const int64_t per_tile = 2 * int64_t(kPackBlockN) * 128;  // one packed tile: 32 KB
+  return static_cast<int>(std::clamp<int64_t>(budget / (int64_t(std::max(grid, 1)) * per_tile), 2, 16));
 }
 }  // namespace swg
 
@@ -625,8 +638,9 @@ swiglu_status_t swiglu_plan_string(int64_t M, int64_t K, int64_t N, int variant,
   if (st != SWIGLU_OK) return st;
   if (pl.variant == SWIGLU_VARIANT_SMALL_M)
     std::snprintf(buf, buflen,
-                  "small_m mt=%d stages=%d tiles=%d groups=%d splits=%d grid=%d sms=%d", pl.mt,
-                  pl.stages, pl.tiles, pl.mgroups, pl.splits, pl.grid, d->sm_count);
+                  "small_m mt=%d stages=%d tiles=%d groups=%d splits=%d grid=%d l2_prefetch=%d sms=%d",
+                  pl.mt, pl.stages, pl.tiles, pl.mgroups, pl.splits, pl.grid,
+                  swg::small_m_l2_prefetch(pl.grid, pl.splits), d->sm_count);
   else if (pl.variant == SWIGLU_VARIANT_SEQUENTIAL)
     std::snprintf(buf, buflen, "sequential bn=%d stages=%d tiles=%d grid=%d group_m=%d sms=%d",
                   pl.bn, pl.stages, pl.tiles, pl.grid, pl.group_m, d->sm_count);

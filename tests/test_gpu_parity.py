@@ -229,6 +229,30 @@ def test_repeated_calls_are_identical(native):
     assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
 
 
+@pytest.mark.parametrize("M,K,N", [(16, 1024, 2048), (40, 896, 4864)])
+def test_forward_sees_weights_repacked_in_place(native, M, K, N):
+    # One packed buffer, two weight sets, alternately packed into it and used by
+    # a forward call on one stream with no synchronisation in between. The decode
+    # kernel stages weight tiles in L2 before it waits for the kernel ahead of it;
+    # every call must still compute with the weights packed just before it.
+    from oracle import compare
+    a, w1, w2 = make_inputs(M, K, N, seed=91)
+    _, v1, v2 = make_inputs(M, K, N, seed=92)
+    ad, w1d, w2d, v1d, v2d = to_dev(a, w1, w2, v1, v2)
+    wp = native.swiglu_pack_weights(w1d, w2d)
+    ys = []
+    for i in range(6):
+        if i:
+            native.swiglu_pack_weights(*((v1d, v2d) if i % 2 else (w1d, w2d)), Wpacked=wp)
+        ys.append(native.swiglu_forward(ad, wp, N))
+    native.swiglu_check_device_status()
+    ab = bf16_bits(a)
+    refs = [swiglu_f64(ab, bf16_bits(w1), bf16_bits(w2)), swiglu_f64(ab, bf16_bits(v1), bf16_bits(v2))]
+    for i, y in enumerate(ys):
+        rep = compare.report(bf16_bits(y.cpu()), refs[i % 2])
+        assert rep["tolerance_pass"] and rep["nonfinite"] == 0, (i, rep)
+
+
 def test_forward_from_host_buffers(native):
     M, K, N = 16, 512, 640
     a, w1, w2 = make_inputs(M, K, N, seed=14)
