@@ -16,7 +16,8 @@ JSON line (rank 0). Metric: TFLOP/s counted as 4*M*K*N per step.
   launches: one launch per step), against the measured peaks in
   MEASURED_PEAKS.json.
 * e2e: the same metric through swiglu_forward_from_host, with each step's
-  activations copied from pinned host memory and its output copied back.
+  activations copied from pinned host memory and its output copied back;
+  alternate steps go to two streams with their own staging buffers.
 * cpu_baseline: the CPU oracle (float64) on a bounded sample of the workload.
 * --impl reference: the CPU oracle timed as the reference arm (the method has
   no runnable reference implementation).
@@ -368,24 +369,33 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     a_host = [a_cpu.pin_memory()] + [a_cpu.clone().pin_memory() for _ in range(min(copies, 4) - 1)]
     y_host = [torch.empty(M, out_cols, dtype=torch.bfloat16).pin_memory()
               for _ in range(len(a_host))]
-    a_dev = torch.empty(*a_cpu.shape, dtype=a_cpu.dtype, device=dev)
-    y_dev = torch.empty(M, out_cols, dtype=torch.bfloat16, device=dev)
+    # Two streams, each with its own device staging buffers, take alternate
+    # steps (as a serving loop would): one step's host copies overlap the
+    # neighbouring steps' kernels, and every step's copies stay in the region.
+    e2e_streams = [stream, torch.cuda.Stream(device=dev)]
+    a_dev = [torch.empty(*a_cpu.shape, dtype=a_cpu.dtype, device=dev) for _ in e2e_streams]
+    y_dev = [torch.empty(M, out_cols, dtype=torch.bfloat16, device=dev) for _ in e2e_streams]
     e2e_steps = steps
 
     def e2e_step(i):
         j = i % len(a_host)
+        b = i % len(e2e_streams)
+        st = e2e_streams[b]
         if down:  # host copies through torch around the down-projection call
-            a_dev.copy_(a_host[j], non_blocking=True)
-            sg.swiglu_down_forward(a_dev, wps[i % copies], K, R=Rs[i % copies], Out=y_dev,
-                                   stream=stream)
-            y_host[j].copy_(y_dev, non_blocking=True)
+            with torch.cuda.stream(st):
+                a_dev[b].copy_(a_host[j], non_blocking=True)
+                sg.swiglu_down_forward(a_dev[b], wps[i % copies], K, R=Rs[i % copies],
+                                       Out=y_dev[b], stream=st)
+                y_host[j].copy_(y_dev[b], non_blocking=True)
         elif fp8:  # host copies through torch around the FP8 call
-            a_dev.copy_(a_host[j], non_blocking=True)
-            sg.swiglu_forward_fp8(a_dev, wps[i % copies], N, s_a, s_1, s_2, Y=y_dev, stream=stream)
-            y_host[j].copy_(y_dev, non_blocking=True)
+            with torch.cuda.stream(st):
+                a_dev[b].copy_(a_host[j], non_blocking=True)
+                sg.swiglu_forward_fp8(a_dev[b], wps[i % copies], N, s_a, s_1, s_2, Y=y_dev[b],
+                                      stream=st)
+                y_host[j].copy_(y_dev[b], non_blocking=True)
         else:
-            sg.swiglu_forward_from_host(a_host[j], wps[i % copies], N, y_host[j], a_dev, y_dev,
-                                        stream=stream)
+            sg.swiglu_forward_from_host(a_host[j], wps[i % copies], N, y_host[j], a_dev[b],
+                                        y_dev[b], stream=st)
 
     for i in range(max(3, args.warmup // 10)):
         e2e_step(i)
@@ -401,7 +411,10 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     e2e = {"value": round(aggregate(flops, e2e_steps, e2e_s, world), 3), "unit": "TFLOP/s",
            "h2d_bytes_per_step": a_cpu.numel() * a_cpu.element_size(),
            "d2h_bytes_per_step": 2 * M * out_cols,
-           "steps": e2e_steps, "api": "swiglu_forward_from_host"}
+           "steps": e2e_steps, "streams": len(e2e_streams),
+           "api": ("pinned-host copies + swiglu_down_forward" if down else
+                   "pinned-host copies + swiglu_forward_fp8" if fp8 else
+                   "swiglu_forward_from_host")}
 
     out = {
         "metric": METRIC_DOWN if down else METRIC, "value": round(value, 3), "unit": "TFLOP/s",
