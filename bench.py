@@ -94,15 +94,20 @@ def profiled_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from a committed ncu summary of this kernel source."""
     stamp = source_stamp()
     for path in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
-        fields = {}
+        # "bench-key k=v" lines: one key per line (one record per file), or a
+        # whole record of space-separated k=v pairs on one line
+        records, single = [], {}
         with open(path) as f:
             for line in f:
-                if line.startswith("bench-key "):
-                    k, _, v = line[len("bench-key "):].strip().partition("=")
-                    fields[k.strip()] = v.strip()
-        if (fields.get("kernel") == kernel and fields.get("workload") == workload
-                and fields.get("source_stamp") == stamp and "dram_bytes_per_launch" in fields):
-            return float(fields["dram_bytes_per_launch"]), os.path.relpath(path, ROOT)
+                if not line.startswith("bench-key "):
+                    continue
+                pairs = [kv.partition("=") for kv in line[len("bench-key "):].split()]
+                rec = {k.strip(): v.strip() for k, _, v in pairs if k}
+                (records.append(rec) if len(rec) > 1 else single.update(rec))
+        for fields in records + [single]:
+            if (fields.get("kernel") == kernel and fields.get("workload") == workload
+                    and fields.get("source_stamp") == stamp and "dram_bytes_per_launch" in fields):
+                return float(fields["dram_bytes_per_launch"]), os.path.relpath(path, ROOT)
     return None, None
 
 
@@ -339,13 +344,14 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     tensor_sus = peaks.get("bf16_tflops_sustained")
     tensor_sus = tensor_sus * (2.0 if fp8 else 1.0) if tensor_sus else None
     hbm_bound = flops / alg_bytes < tensor_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    kernel = ("fused_small_m_kernel" if plan.startswith("small_m") else
-              "fused_large_m_pair_kernel" if plan.startswith("large_m_pair") else
-              "fused_sequential_kernel" if plan.startswith("sequential") else
+    base = plan.split(" ", 1)[1] if plan.startswith(("down ", "fp8 ")) else plan
+    kernel = ("fused_small_m_kernel" if base.startswith("small_m") else
+              "fused_large_m_pair_kernel" if base.startswith("large_m_pair") else
+              "fused_sequential_kernel" if base.startswith("sequential") else
               "fused_large_m_kernel")
+    if down or fp8:  # the template instance: <fp8> is E4M3 inputs, <down> the down-projection
+        kernel += "<down>" if down else "<fp8>"
     traffic, traffic_src = profiled_traffic(kernel, w.name)
-    if fp8:
-        traffic, traffic_src = None, None  # the committed ncu summaries cover the bf16 kernels
     if hbm_bound:
         achieved = alg_bytes / avg_launch / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
