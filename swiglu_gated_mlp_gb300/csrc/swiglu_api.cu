@@ -43,6 +43,18 @@ int64_t env_int(const char* name, int64_t dflt) {
   return (end && *end == '\0') ? static_cast<int64_t>(x) : dflt;
 }
 
+// Row tiles (of 256 rows) per group in the CTA-pair kernels' tile order: the
+// 76 pairs sweep a group's rows before moving to the next column blocks. 16
+// rows tiles read the least DRAM in a sweep of 4 to 32 on the 72B gate/up
+// shapes (bf16 and FP8) and on the down-projections (K = 18944 to 29568),
+// where no grouping keeps a wave's A and W panels in L2; smaller shapes have
+// at most 16 row tiles, one group. SWIGLU_PAIR_GROUP_M=g forces g.
+int64_t pair_group_rows(int64_t row_tiles) {
+  static const int64_t forced = env_int("SWIGLU_PAIR_GROUP_M", 0);
+  const int64_t g = forced > 0 ? forced : 16;
+  return std::max<int64_t>(1, std::min(g, row_tiles));
+}
+
 // Largest M for which AUTO picks the small-M (weights-as-MMA-M) kernel.
 int64_t small_m_max() {
   static const int64_t v = env_int("SWIGLU_SMALL_M_MAX", 32);
@@ -338,9 +350,7 @@ swiglu_status_t make_plan(int64_t M, int64_t K, int64_t N, int variant, const De
     const int64_t pm = (M + 2 * swg::kTileM - 1) / (2 * swg::kTileM);  // 256-row tiles
     const int64_t ptiles = pm * (np / swg::kPackBlockN);
     if (ptiles > 2147483647) return SWIGLU_ERR_UNSUPPORTED;
-    int64_t group = (48ll << 20) / (int64_t(2 * swg::kTileM) * K * elem_bytes);
-    if (group < 1) group = 1;
-    if (group > pm) group = pm;
+    const int64_t group = pair_group_rows(pm);
     pl->bn = swg::kPackBlockN;
     pl->stages = swg::large_m_pair_stages();
     pl->tiles_m = static_cast<int>(pm);
@@ -880,9 +890,7 @@ swiglu_status_t swiglu_down_forward(const void* Y, const void* W3packed, const v
     const int64_t pm = (M + 2 * swg::kTileM - 1) / (2 * swg::kTileM);
     const int64_t tiles = pm * blocks;
     if (tiles > 2147483647) return SWIGLU_ERR_UNSUPPORTED;
-    int64_t group = (48ll << 20) / (int64_t(2 * swg::kTileM) * N * 2);
-    if (group < 1) group = 1;
-    if (group > pm) group = pm;
+    const int64_t group = pair_group_rows(pm);
     if (!encode_2d(&p.tmap_a, Y, N, M, N * 2, swg::kBlockK, swg::kTileM,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_packed_down(&p.tmap_w, W3packed, N, H, swg::kPackBlockN) ||
