@@ -270,8 +270,7 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
         Rs = [r0] + [r0.clone() for _ in range(copies - 1)]
     variant = VARIANTS[args.variant]
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    down_small = M <= 64 or (M <= 128 and 2 * (-(-K // 256)) <= sms)
-    plan = (("down small_m" if down_small else "down large_m_pair") if down else
+    plan = (sg.swiglu_down_plan_string(M, N, K) if down else
             ("fp8 " + ("small_m" if (M <= 32 or (M <= 64 and 2 * (-(-N // 128)) <= sms))
                        else "large_m_pair")) if fp8 else
             sg.swiglu_plan_string(M, K, N, variant))

@@ -218,6 +218,15 @@ SWIGLU_API swiglu_status_t swiglu_down_forward(const void* Y, const void* W3pack
                                                swiglu_stream_t stream);
 
 /*
+ * swiglu_down_plan_string: the kernel and launch shape swiglu_down_forward
+ * chooses for (M, N, H) on the current device, as text ("down small_m ..." or
+ * "down large_m_pair ..."). buf NULL or buflen 0: INVALID_ARG; no usable
+ * device: NO_DEVICE; bad shape: as swiglu_down_forward.
+ */
+SWIGLU_API swiglu_status_t swiglu_down_plan_string(int64_t M, int64_t N, int64_t H, char* buf,
+                                                   size_t buflen);
+
+/*
  * Allocation-free forward for callers that cannot call cudaMalloc: code that
  * runs while a stream is being captured into a CUDA graph (allocation is not
  * allowed there), serving runtimes that reserve all device memory for their

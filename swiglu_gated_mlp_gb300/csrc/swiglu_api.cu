@@ -294,6 +294,35 @@ void decode_split_plan(int64_t M, int64_t blocks, int64_t kslices, const DeviceS
   }
 }
 
+struct DownPlan {
+  bool decode = false;
+  int mt = 0, mgroups = 1, stages = 0, splits = 1, grid = 0;  // splits: decode clusters
+  int64_t blocks = 0, pm = 0, tiles = 0, group = 1;
+};
+
+// The down-projection's kernel and launch shape.
+swiglu_status_t make_down_plan(int64_t M, int64_t N, int64_t H, const DeviceState* d,
+                               DownPlan* dp) {
+  *dp = DownPlan{};
+  dp->blocks = padded_h(H) / 256;  // 256 output columns per block
+  const int64_t ks = k_slices(N);
+  // decode kernel for few tokens, or up to 128 tokens when there are few output
+  // blocks for the SMs (K then splits over clusters); CTA pairs otherwise
+  if (M <= 64 || (M <= swg::kTileM && dp->blocks * 2 <= d->sm_count)) {
+    dp->decode = true;
+    decode_split_plan(M, dp->blocks, ks, d, &dp->mt, &dp->mgroups, &dp->stages, &dp->splits);
+    dp->grid = static_cast<int>(dp->blocks * dp->mgroups * dp->splits);
+    return SWIGLU_OK;
+  }
+  if (d->max_pairs < 1) return SWIGLU_ERR_UNSUPPORTED;
+  dp->pm = (M + 2 * swg::kTileM - 1) / (2 * swg::kTileM);
+  dp->tiles = dp->pm * dp->blocks;
+  if (dp->tiles > 2147483647) return SWIGLU_ERR_UNSUPPORTED;
+  dp->group = pair_group_rows(dp->pm);
+  dp->grid = 2 * static_cast<int>(dp->tiles < d->max_pairs ? dp->tiles : d->max_pairs);
+  return SWIGLU_OK;
+}
+
 // `d` may be null (allocation-free entry point): no SM count, no cluster data.
 swiglu_status_t make_plan(int64_t M, int64_t K, int64_t N, int variant, const DeviceState* d,
                           Plan* pl, int elem_bytes = 2) {
@@ -844,6 +873,29 @@ swiglu_status_t swiglu_pack_down_weights(const void* W3, void* W3packed, int64_t
   return SWIGLU_OK;
 }
 
+swiglu_status_t swiglu_down_plan_string(int64_t M, int64_t N, int64_t H, char* buf,
+                                        size_t buflen) {
+  if (!buf || buflen == 0) return SWIGLU_ERR_INVALID_ARG;
+  buf[0] = '\0';
+  swiglu_status_t st = check_shape(M, N, H);
+  if (st != SWIGLU_OK) return st;
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != SWIGLU_OK) return st;
+  DownPlan dp;
+  st = make_down_plan(M < 1 ? 1 : M, N, H, d, &dp);
+  if (st != SWIGLU_OK) return st;
+  if (dp.decode)
+    std::snprintf(buf, buflen, "down small_m mt=%d stages=%d blocks=%lld groups=%d splits=%d grid=%d sms=%d",
+                  dp.mt, dp.stages, static_cast<long long>(dp.blocks), dp.mgroups, dp.splits,
+                  dp.grid, d->sm_count);
+  else
+    std::snprintf(buf, buflen, "down large_m_pair tiles=%lld group_m=%lld grid=%d max_pairs=%d sms=%d",
+                  static_cast<long long>(dp.tiles), static_cast<long long>(dp.group), dp.grid,
+                  d->max_pairs, d->sm_count);
+  return SWIGLU_OK;
+}
+
 swiglu_status_t swiglu_down_forward(const void* Y, const void* W3packed, const void* R, void* Out,
                                     int64_t M, int64_t N, int64_t H, swiglu_stream_t stream) {
   swiglu_status_t st = check_shape(M, N, H);
@@ -860,16 +912,18 @@ swiglu_status_t swiglu_down_forward(const void* Y, const void* W3packed, const v
   DeviceState* d = nullptr;
   st = device_state(&d);
   if (st != SWIGLU_OK) return st;
+  DownPlan dp;
+  st = make_down_plan(M, N, H, d, &dp);
+  if (st != SWIGLU_OK) return st;
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  const int64_t blocks = padded_h(H) / 256;  // 256 output columns per block
-  const int64_t ks = k_slices(N);
   cudaError_t err;
-  // decode kernel for few tokens, or up to 128 tokens when there are few output
-  // blocks for the SMs (K then splits over clusters); CTA pairs otherwise
-  if (M <= 64 || (M <= swg::kTileM && blocks * 2 <= d->sm_count)) {
+  if (dp.decode) {
     // decode: weights as the MMA M side, K split over clusters when blocks are few
     swg::SmallMParams p{};
-    decode_split_plan(M, blocks, ks, d, &p.mt, &p.mgroups, &p.stages, &p.splits);
+    p.mt = dp.mt;
+    p.mgroups = dp.mgroups;
+    p.stages = dp.stages;
+    p.splits = dp.splits;
     if (!encode_2d(&p.tmap_x, Y, N, M, N * 2, swg::kBlockK, p.mt, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_packed_down(&p.tmap_w, W3packed, N, H, 256))
       return SWIGLU_ERR_CUDA;
@@ -879,18 +933,13 @@ swiglu_status_t swiglu_down_forward(const void* Y, const void* W3packed, const v
     p.M = static_cast<int>(M);
     p.K = static_cast<int>(N);
     p.N = static_cast<int>(H);
-    p.grid = static_cast<int>(blocks * p.mgroups * p.splits);
+    p.grid = dp.grid;
     p.status = d->status;
     p.timeout_ns = g_timeout_ns.load();
     p.inject_stall = g_inject.load();
     err = swg::launch_small_m(p, cs);
   } else {
-    if (d->max_pairs < 1) return SWIGLU_ERR_UNSUPPORTED;
     swg::LargeMParams p{};
-    const int64_t pm = (M + 2 * swg::kTileM - 1) / (2 * swg::kTileM);
-    const int64_t tiles = pm * blocks;
-    if (tiles > 2147483647) return SWIGLU_ERR_UNSUPPORTED;
-    const int64_t group = pair_group_rows(pm);
     if (!encode_2d(&p.tmap_a, Y, N, M, N * 2, swg::kBlockK, swg::kTileM,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_packed_down(&p.tmap_w, W3packed, N, H, swg::kPackBlockN) ||
@@ -899,11 +948,11 @@ swiglu_status_t swiglu_down_forward(const void* Y, const void* W3packed, const v
     p.M = static_cast<int>(M);
     p.K = static_cast<int>(N);
     p.N = static_cast<int>(H);
-    p.tiles_m = static_cast<int>(pm);
-    p.tiles_n = static_cast<int>(blocks);
-    p.group_m = static_cast<int>(group);
+    p.tiles_m = static_cast<int>(dp.pm);
+    p.tiles_n = static_cast<int>(dp.blocks);
+    p.group_m = static_cast<int>(dp.group);
     p.bn = swg::kPackBlockN;
-    p.grid = 2 * static_cast<int>(tiles < d->max_pairs ? tiles : d->max_pairs);
+    p.grid = dp.grid;
     p.down = 1;
     p.residual = R;
     p.status = d->status;

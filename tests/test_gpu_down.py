@@ -82,3 +82,8 @@ def test_down_qwen7b_shape(native, M):
     rows = sample_rows(M, 64, seed=M)
     rep = run_down(native, M, 18944, 3584, seed=7 + M, rows=rows)
     assert rep["mismatch_rate"] == 0.0
+
+
+def test_down_plan_string_names_the_kernel(native):
+    assert native.swiglu_down_plan_string(16, 18944, 3584).startswith("down small_m")
+    assert native.swiglu_down_plan_string(4096, 18944, 3584).startswith("down large_m_pair")
