@@ -51,3 +51,33 @@ def test_fused_has_no_mismatch_and_unfused_rate_is_reported(native, name, record
           f"relative>1% {unfused['relative_mismatch_rate']:.6f})")
     assert fused["mismatch_rate"] == 0.0 and fused["tolerance_pass"], fused
     assert unfused["nonfinite"] == 0
+
+
+@pytest.mark.parametrize("name", CASES)
+def test_unfused_error_is_the_bf16_rounding_of_the_intermediates(native, name):
+    # torch eager against the model that rounds Gate, Up, SiLU(Gate) and the
+    # product to bf16 once each: the same mismatch rates and nearly all bits,
+    # with cuBLAS's reduced-precision reductions allowed or not.
+    from oracle.unfused_ref import unfused_bf16
+    w = WORKLOADS[name]
+    a, w1, w2 = make_workload_inputs(w)
+    ad, w1d, w2d = a.cuda(), w1.cuda(), w2.cuda()
+    rows = sample_rows(w.M, 64, seed=w.seed)
+    idx = torch.from_numpy(rows).cuda()
+    ab, w1b, w2b = bf16_bits(a), bf16_bits(w1), bf16_bits(w2)
+    ref = swiglu_f64(ab, w1b, w2b, rows=rows)
+    model = unfused_bf16(ab, w1b, w2b, rows=rows)
+    rep_model = compare.report(model, ref)
+    flag = torch.backends.cuda.matmul.allow_bf16_reduced_precision_reduction
+    try:
+        outs = []
+        for allow in (True, False):
+            torch.backends.cuda.matmul.allow_bf16_reduced_precision_reduction = allow
+            outs.append(bf16_bits((torch.nn.functional.silu(ad @ w1d) * (ad @ w2d))[idx].cpu()))
+    finally:
+        torch.backends.cuda.matmul.allow_bf16_reduced_precision_reduction = flag
+    for eager in outs:
+        rep = compare.report(eager, ref)
+        assert float((eager == model).mean()) >= 0.99
+        assert abs(rep["mismatch_rate"] - rep_model["mismatch_rate"]) <= 5e-5
+        assert abs(rep["relative_mismatch_rate"] - rep_model["relative_mismatch_rate"]) <= 2e-4
