@@ -90,3 +90,21 @@ def test_reference_arm_non_zero_rank_does_nothing():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
                         "--steps", "2"], capture_output=True, text=True, timeout=120, env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_profiled_traffic_reads_both_record_forms(tmp_path, monkeypatch):
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    stamp = bench.source_stamp()
+    (prof / "one.md").write_text(
+        "text\nbench-key kernel=k_a\nbench-key workload=w1\n"
+        f"bench-key source_stamp={stamp}\nbench-key dram_bytes_per_launch=100\n")
+    (prof / "many.md").write_text(
+        f"bench-key kernel=k_b<fp8> workload=w1 source_stamp={stamp} dram_bytes_per_launch=200\n"
+        f"bench-key kernel=k_b<fp8> workload=w2 source_stamp=0000 dram_bytes_per_launch=300\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "source_stamp", lambda: stamp)
+    assert bench.profiled_traffic("k_a", "w1")[0] == 100.0
+    assert bench.profiled_traffic("k_b<fp8>", "w1")[0] == 200.0
+    assert bench.profiled_traffic("k_b<fp8>", "w2") == (None, None)  # stale stamp
+    assert bench.profiled_traffic("k_a", "w2") == (None, None)
