@@ -146,6 +146,23 @@ def test_extreme_shapes_match_oracle(native, M, K, N, variant):
     check_against_oracle(native, M, K, N, seed=M + 2 * K + N, variant=variant, rows=rows)
 
 
+# The limits of the boundary: K or N at 2^21 (the largest the ABI accepts),
+# and the smallest K and N (8, one 16-byte row) on every kernel.
+MAX_CASES = [(1, 1 << 21, 128), (3, 64, 1 << 21)]
+
+
+@pytest.mark.parametrize("M,K,N", MAX_CASES)
+def test_largest_k_and_n_match_oracle(native, M, K, N):
+    check_against_oracle(native, M, K, N, seed=M + 5, variant=AUTO)
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("variant", [AUTO, LARGE, SMALL, PAIR, SEQ])
+@pytest.mark.parametrize("M", [1, 9, 130])
+def test_smallest_k_and_n_match_oracle(native, variant, M):
+    check_against_oracle(native, M, 8, 8, seed=M + variant, variant=variant)
+
+
 # ------------------------------------------------------- special values ----
 
 @pytest.mark.parametrize("variant", [LARGE, SMALL])
