@@ -634,6 +634,59 @@ def run_reference(args, w: Workload, world: int, rank: int):
     }
 
 
+def library_peak(kind: str, n: int = 8192, seconds: float = 4.0) -> dict:
+    """cuBLAS(Lt) GEMM throughput on this GPU, as context for the roofline peaks.
+
+    bf16: torch.matmul of two n x n bf16 matrices. fp8: torch._scaled_mm of two
+    n x n E4M3 matrices (unit scales, bf16 output). FLOPs 2 n^3 per call.
+    Burst: the best of 10 single calls (CUDA events); sustained: calls back to
+    back for `seconds`, which on this part runs at the power cap.
+    """
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if kind == "fp8":
+        a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn).t()  # column-major operand
+        one = torch.tensor(1.0, device=dev)
+
+        def fn():
+            return torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+    else:
+        a = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+        b = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+
+        def fn():
+            return a @ b
+    for _ in range(5):
+        fn()
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1) * 1e-3)
+    sampler = ClockSampler(dev.index)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    calls = 0
+    with sampler:
+        t0 = time.perf_counter()
+        e0.record()
+        while time.perf_counter() - t0 < seconds:
+            for _ in range(20):
+                fn()
+            calls += 20
+            torch.cuda.synchronize()
+        e1.record()
+        torch.cuda.synchronize()
+    flop = 2.0 * n ** 3
+    return {"library_peak": "torch._scaled_mm (E4M3)" if kind == "fp8" else "torch.matmul (bf16)",
+            "n": n, "unit": "TFLOP/s", "burst": round(flop / best / 1e12, 1),
+            "sustained": round(flop * calls / (e0.elapsed_time(e1) * 1e-3) / 1e12, 1),
+            "sustained_seconds": seconds, "clocks": sampler.summary()}
+
+
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -656,8 +709,15 @@ def main(argv=None):
                    help="time per-call launches instead of CUDA graph replay")
     p.add_argument("--compare-unfused", action="store_true",
                    help="also time the unfused PyTorch eager path and report the derived metrics")
+    p.add_argument("--library-peak", choices=["bf16", "fp8"], default=None,
+                   help="instead of the op: the library GEMM's throughput for context "
+                        "(bf16: torch.matmul; fp8: torch._scaled_mm, E4M3), 8192^3, burst "
+                        "(best of 10) and sustained (4 s back to back), with clocks")
     args = p.parse_args(argv)
     args.warmup = max(args.warmup, 3)
+    if args.library_peak:
+        print(json.dumps(library_peak(args.library_peak)), flush=True)
+        return
     w = workload_by_name(args.workload)
     if args.impl == "reference":
         # rank 0 alone runs the CPU reference; other ranks exit without work
