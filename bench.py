@@ -33,6 +33,7 @@ os.environ.setdefault("OPENBLAS_NUM_THREADS", str(_CORES))
 os.environ.setdefault("OMP_NUM_THREADS", str(_CORES))
 
 import argparse  # noqa: E402
+import dataclasses  # noqa: E402
 import glob  # noqa: E402
 import hashlib  # noqa: E402
 import json  # noqa: E402
@@ -269,10 +270,8 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
         r0 = r_cpu.to(dev)
         Rs = [r0] + [r0.clone() for _ in range(copies - 1)]
     variant = VARIANTS[args.variant]
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     plan = (sg.swiglu_down_plan_string(M, N, K) if down else
-            ("fp8 " + ("small_m" if (M <= 32 or (M <= 64 and 2 * (-(-N // 128)) <= sms))
-                       else "large_m_pair")) if fp8 else
+            sg.swiglu_plan_string_fp8(M, K, N) if fp8 else
             sg.swiglu_plan_string(M, K, N, variant))
     stream = torch.cuda.current_stream(dev)
 
@@ -713,12 +712,18 @@ def main(argv=None):
                    help="instead of the op: the library GEMM's throughput for context "
                         "(bf16: torch.matmul; fp8: torch._scaled_mm, E4M3), 8192^3, burst "
                         "(best of 10) and sustained (4 s back to back), with clocks")
+    p.add_argument("--m", type=int, default=0,
+                   help="token count in place of the workload's M (same K, N and seed; the "
+                        "workload name gets an @M= suffix)")
     args = p.parse_args(argv)
     args.warmup = max(args.warmup, 3)
     if args.library_peak:
         print(json.dumps(library_peak(args.library_peak)), flush=True)
         return
     w = workload_by_name(args.workload)
+    if args.m > 0:
+        w = dataclasses.replace(w, name=f"{w.name}@M={args.m}", M=args.m,
+                                note=f"{w.note}; M set to {args.m}")
     if args.impl == "reference":
         # rank 0 alone runs the CPU reference; other ranks exit without work
         world = int(os.environ.get("WORLD_SIZE", "1"))

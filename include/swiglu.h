@@ -192,6 +192,14 @@ SWIGLU_API swiglu_status_t swiglu_forward_fp8(const void* A, const void* Wpacked
                                               int64_t M, int64_t K, int64_t N, float scale_a,
                                               float scale_w1, float scale_w2,
                                               swiglu_stream_t stream);
+/*
+ * swiglu_plan_string_fp8: the kernel and launch shape swiglu_forward_fp8
+ * chooses for (M, K, N) on the current device, as text ("fp8 small_m ..." or
+ * "fp8 large_m_pair ..."). buf NULL or buflen 0: INVALID_ARG; K not a
+ * multiple of 16: UNSUPPORTED; no usable device: NO_DEVICE.
+ */
+SWIGLU_API swiglu_status_t swiglu_plan_string_fp8(int64_t M, int64_t K, int64_t N, char* buf,
+                                                  size_t buflen);
 
 /*
  * The gated MLP's down-projection, the step after Y in the models the pages

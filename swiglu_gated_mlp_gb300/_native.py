@@ -67,6 +67,8 @@ lib.swiglu_down_forward.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]
 lib.swiglu_down_forward.restype = _int
 lib.swiglu_down_plan_string.argtypes = [_i64, _i64, _i64, ctypes.c_char_p, _sz]
 lib.swiglu_down_plan_string.restype = _int
+lib.swiglu_plan_string_fp8.argtypes = [_i64, _i64, _i64, ctypes.c_char_p, _sz]
+lib.swiglu_plan_string_fp8.restype = _int
 lib.swiglu_forward_noalloc.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp]
 lib.swiglu_forward_noalloc.restype = _int
 lib.swiglu_testing_inject_stall.argtypes = [_int, _u32]
@@ -260,6 +262,12 @@ def swiglu_pack_down_weights(W3: torch.Tensor, W3packed: torch.Tensor | None = N
                                             _stream_handle(stream, W3.device)),
                "swiglu_pack_down_weights")
     return W3packed
+
+
+def swiglu_plan_string_fp8(M: int, K: int, N: int) -> str:
+    buf = ctypes.create_string_buffer(256)
+    _check(lib.swiglu_plan_string_fp8(int(M), int(K), int(N), buf, 256), "swiglu_plan_string_fp8")
+    return buf.value.decode()
 
 
 def swiglu_down_plan_string(M: int, N: int, H: int) -> str:

@@ -335,11 +335,18 @@ swiglu_status_t make_plan(int64_t M, int64_t K, int64_t N, int variant, const De
   if (variant == SWIGLU_VARIANT_AUTO) {
     const int64_t nb = padded_n(N) / swg::kPackBlockN;
     const int64_t tiles128 = ((M + swg::kTileM - 1) / swg::kTileM) * nb;
+    // From a sweep of M = 1..128 on the 7B and 32B shapes (every kernel, CUDA
+    // events): the decode kernel up to 32 tokens, up to 64 on narrow N (K split
+    // over clusters), up to 80 when the column blocks fill most SMs at one CTA
+    // each; single CTAs up to 128 tokens; CTA pairs above when the 128-row
+    // tiles fill the SMs.
     if (M <= small_m_max() && M <= 256) {
       variant = SWIGLU_VARIANT_SMALL_M;                  // decode: stream the weights once
     } else if (M <= 64 && sm_count > 0 && nb * 2 <= sm_count) {
       variant = SWIGLU_VARIANT_SMALL_M;                  // few column blocks: split K in clusters
-    } else if (max_pairs > 0 && (M <= swg::kTileM ? nb > sm_count : tiles128 >= sm_count)) {
+    } else if (M <= 80 && sm_count > 0 && nb <= sm_count && nb * 2 > sm_count) {
+      variant = SWIGLU_VARIANT_SMALL_M;                  // one resident CTA per column block
+    } else if (M > swg::kTileM && max_pairs > 0 && tiles128 >= sm_count) {
       variant = SWIGLU_VARIANT_LARGE_M_PAIR;             // 256-row tiles on CTA pairs
     } else {
       variant = SWIGLU_VARIANT_LARGE_M;
@@ -548,6 +555,38 @@ swiglu_status_t noalloc_state(NoAllocState** out) {
 
 }  // namespace
 
+namespace {
+// Text form of a plan (swiglu_plan_string, swiglu_plan_string_fp8).
+void format_plan(const Plan& pl, const DeviceState& d, const char* prefix, char* buf,
+                 size_t buflen) {
+  if (pl.variant == SWIGLU_VARIANT_SMALL_M)
+    std::snprintf(buf, buflen,
+                  "%ssmall_m mt=%d stages=%d tiles=%d groups=%d splits=%d grid=%d l2_prefetch=%d sms=%d",
+                  prefix, pl.mt, pl.stages, pl.tiles, pl.mgroups, pl.splits, pl.grid,
+                  swg::small_m_l2_prefetch(pl.grid, pl.splits), d.sm_count);
+  else if (pl.variant == SWIGLU_VARIANT_SEQUENTIAL)
+    std::snprintf(buf, buflen, "%ssequential bn=%d stages=%d tiles=%d grid=%d group_m=%d sms=%d",
+                  prefix, pl.bn, pl.stages, pl.tiles, pl.grid, pl.group_m, d.sm_count);
+  else if (pl.variant == SWIGLU_VARIANT_LARGE_M_PAIR)
+    std::snprintf(buf, buflen,
+                  "%slarge_m_pair bn=%d stages=%d tiles=%d grid=%d group_m=%d max_pairs=%d sms=%d",
+                  prefix, pl.bn, pl.stages, pl.tiles, pl.grid, pl.group_m, d.max_pairs, d.sm_count);
+  else
+    std::snprintf(buf, buflen, "%slarge_m bn=%d stages=%d tiles=%d grid=%d group_m=%d sms=%d",
+                  prefix, pl.bn, pl.stages, pl.tiles, pl.grid, pl.group_m, d.sm_count);
+}
+
+// The FP8 entry point's kernel: as for bf16, the decode kernel up to 32 tokens,
+// up to 64 on narrow N, up to 80 when the column blocks fill most SMs at one
+// CTA each (there it beat the pair kernel by 4-11 % at M = 40-80 on the 7B
+// shape); the CTA-pair kernel otherwise (there is no single-CTA FP8 kernel).
+bool fp8_uses_decode(int64_t M, int64_t N, const DeviceState& d) {
+  const int64_t nb = padded_n(N) / swg::kPackBlockN;
+  return M <= 32 || (M <= 64 && nb * 2 <= d.sm_count) ||
+         (M <= 80 && nb <= d.sm_count && nb * 2 > d.sm_count) || d.max_pairs < 1;
+}
+}  // namespace
+
 extern "C" {
 
 size_t swiglu_packed_weight_bytes(int64_t K, int64_t N) {
@@ -675,21 +714,27 @@ swiglu_status_t swiglu_plan_string(int64_t M, int64_t K, int64_t N, int variant,
   Plan pl;
   st = make_plan(M < 1 ? 1 : M, K, N, variant, d, &pl);
   if (st != SWIGLU_OK) return st;
-  if (pl.variant == SWIGLU_VARIANT_SMALL_M)
-    std::snprintf(buf, buflen,
-                  "small_m mt=%d stages=%d tiles=%d groups=%d splits=%d grid=%d l2_prefetch=%d sms=%d",
-                  pl.mt, pl.stages, pl.tiles, pl.mgroups, pl.splits, pl.grid,
-                  swg::small_m_l2_prefetch(pl.grid, pl.splits), d->sm_count);
-  else if (pl.variant == SWIGLU_VARIANT_SEQUENTIAL)
-    std::snprintf(buf, buflen, "sequential bn=%d stages=%d tiles=%d grid=%d group_m=%d sms=%d",
-                  pl.bn, pl.stages, pl.tiles, pl.grid, pl.group_m, d->sm_count);
-  else if (pl.variant == SWIGLU_VARIANT_LARGE_M_PAIR)
-    std::snprintf(buf, buflen,
-                  "large_m_pair bn=%d stages=%d tiles=%d grid=%d group_m=%d max_pairs=%d sms=%d",
-                  pl.bn, pl.stages, pl.tiles, pl.grid, pl.group_m, d->max_pairs, d->sm_count);
-  else
-    std::snprintf(buf, buflen, "large_m bn=%d stages=%d tiles=%d grid=%d group_m=%d sms=%d",
-                  pl.bn, pl.stages, pl.tiles, pl.grid, pl.group_m, d->sm_count);
+  format_plan(pl, *d, "", buf, buflen);
+  return SWIGLU_OK;
+}
+
+swiglu_status_t swiglu_plan_string_fp8(int64_t M, int64_t K, int64_t N, char* buf,
+                                       size_t buflen) {
+  if (!buf || buflen == 0) return SWIGLU_ERR_INVALID_ARG;
+  buf[0] = '\0';
+  swiglu_status_t st = check_shape(M, K, N);
+  if (st != SWIGLU_OK) return st;
+  if ((K % 16) != 0) return SWIGLU_ERR_UNSUPPORTED;
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != SWIGLU_OK) return st;
+  const int64_t m = M < 1 ? 1 : M;
+  Plan pl;
+  st = make_plan(m, K, N,
+                 fp8_uses_decode(m, N, *d) ? SWIGLU_VARIANT_SMALL_M : SWIGLU_VARIANT_LARGE_M_PAIR, d,
+                 &pl, 1);
+  if (st != SWIGLU_OK) return st;
+  format_plan(pl, *d, "fp8 ", buf, buflen);
   return SWIGLU_OK;
 }
 
@@ -787,11 +832,12 @@ swiglu_status_t swiglu_forward_fp8(const void* A, const void* Wpacked, void* Y, 
   DeviceState* d = nullptr;
   st = device_state(&d);
   if (st != SWIGLU_OK) return st;
-  // As for bf16: the decode kernel for up to 32 tokens, or up to 64 on narrow N;
-  // CTA pairs otherwise (the two FP8 kernels).
+  // As for bf16: the decode kernel for up to 32 tokens, up to 64 on narrow N,
+  // up to 80 when each column block has its own SM; CTA pairs otherwise (the
+  // two FP8 kernels).
   Plan pl;
   const int64_t nb = padded_n(N) / swg::kPackBlockN;
-  const bool small = M <= 32 || (M <= 64 && nb * 2 <= d->sm_count) || d->max_pairs < 1;
+  const bool small = fp8_uses_decode(M, N, *d);
   st = make_plan(M, K, N, small ? SWIGLU_VARIANT_SMALL_M : SWIGLU_VARIANT_LARGE_M_PAIR, d, &pl, 1);
   if (st != SWIGLU_OK) return st;
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);

@@ -108,6 +108,7 @@ def test_valid_call_without_a_device_fails_loudly(native_lib):
     buf = ctypes.create_string_buffer(64)
     assert lib.swiglu_plan_string(16, 64, 64, 0, buf, 64) == native_lib.SWIGLU_ERR_NO_DEVICE
     assert lib.swiglu_down_plan_string(512, 4096, 1024, buf, 64) == native_lib.SWIGLU_ERR_NO_DEVICE
+    assert lib.swiglu_plan_string_fp8(16, 4096, 1024, buf, 64) == native_lib.SWIGLU_ERR_NO_DEVICE
 
 
 def test_down_plan_string_checks_arguments_first(native_lib):
@@ -115,6 +116,8 @@ def test_down_plan_string_checks_arguments_first(native_lib):
     buf = ctypes.create_string_buffer(64)
     assert lib.swiglu_down_plan_string(512, 4096, 1024, None, 0) == native_lib.SWIGLU_ERR_INVALID_ARG
     assert lib.swiglu_down_plan_string(512, 4100, 1024, buf, 64) == native_lib.SWIGLU_ERR_UNSUPPORTED
+    assert lib.swiglu_plan_string_fp8(16, 4104, 1024, buf, 64) == native_lib.SWIGLU_ERR_UNSUPPORTED
+    assert lib.swiglu_plan_string_fp8(16, 4096, 1024, None, 0) == native_lib.SWIGLU_ERR_INVALID_ARG
 
 
 def test_binding_rejects_cpu_tensors(native_lib):

@@ -88,3 +88,12 @@ def test_fp8_rejects_bad_arguments(native):
                                   None) == native.SWIGLU_ERR_UNSUPPORTED  # K % 16
     assert lib.swiglu_forward_fp8(fake, fake * 64, fake * 256, 4, 64, 64, float("nan"), 1.0,
                                   1.0, None) == native.SWIGLU_ERR_INVALID_ARG
+
+
+def test_fp8_plan_string_names_the_kernel(native):
+    # decode kernel up to 80 tokens when the 7B shape's 148 column blocks fill the SMs;
+    # CTA pairs for the 32B shape's 216 blocks above 32 tokens
+    assert native.swiglu_plan_string_fp8(16, 3584, 18944).startswith("fp8 small_m")
+    assert native.swiglu_plan_string_fp8(64, 3584, 18944).startswith("fp8 small_m")
+    assert native.swiglu_plan_string_fp8(48, 5120, 27648).startswith("fp8 large_m_pair")
+    assert native.swiglu_plan_string_fp8(4096, 3584, 18944).startswith("fp8 large_m_pair")

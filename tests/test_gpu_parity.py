@@ -53,7 +53,8 @@ LARGE_CASES = [
     (1000, 256, 512), (513, 896, 4864), (256, 3584, 1024), (384, 72, 8), (2048, 128, 2048),
 ]
 
-AUTO_CASES = [(16, 3584, 1280), (64, 512, 768), (65, 512, 768), (128, 896, 4864), (1024, 1024, 1024)]
+AUTO_CASES = [(16, 3584, 1280), (64, 512, 768), (65, 512, 768), (128, 896, 4864), (1024, 1024, 1024),
+              (48, 256, 18944), (100, 256, 27648)]
 
 
 # Few column blocks: the decode kernel splits K over clusters of 2, 4 or 8 CTAs
@@ -284,6 +285,15 @@ def test_forward_from_host_buffers(native):
     ref = swiglu_f64(bf16_bits(a), bf16_bits(w1), bf16_bits(w2))
     from oracle import compare
     assert compare.report(bf16_bits(y_host), ref)["tolerance_pass"]
+
+
+def test_auto_choice_follows_the_token_sweep(native):
+    # the automatic choice on a 152-SM GB300 (from timing every kernel at M = 1..128)
+    assert native.swiglu_plan_string(48, 3584, 18944).startswith("small_m")     # 148 blocks
+    assert native.swiglu_plan_string(96, 3584, 18944).startswith("large_m bn")
+    assert native.swiglu_plan_string(64, 5120, 27648).startswith("large_m bn")  # 216 blocks
+    assert native.swiglu_plan_string(256, 5120, 27648).startswith("large_m_pair")
+    assert native.swiglu_plan_string(72, 896, 4864).startswith("large_m bn")    # 38 blocks
 
 
 def test_plan_string_names_a_kernel(native):
