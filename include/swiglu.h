@@ -33,6 +33,20 @@
  *
  * Thread safety: calls may be made from several host threads; one-time set-up
  * per device is serialised internally.
+ *
+ * Environment (read once per process; for measurement and tuning, the
+ * defaults are the measured choices):
+ *   SWIGLU_PDL=0            launch without programmatic dependent launch.
+ *   SWIGLU_SMALL_M_MAX=m    largest M for which the automatic choice always
+ *                           takes the decode kernel (default 32).
+ *   SWIGLU_L2_PREFETCH=n    packed tiles each decode CTA stages in L2 before
+ *                           its grid-dependency wait (default: about 64 MB
+ *                           over the grid, at most 16 per CTA; 4 in K-split
+ *                           clusters).
+ *   SWIGLU_PAIR_GROUP_M=g   row tiles per group in the CTA-pair kernels' tile
+ *                           order (default 16).
+ *   SWIGLU_VERBOSE=1        swiglu_check_device_status prints the status record
+ *                           (wait site, block, count) to stderr on a failure.
  */
 #ifndef SWIGLU_H_
 #define SWIGLU_H_
