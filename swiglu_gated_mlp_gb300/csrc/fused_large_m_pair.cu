@@ -279,47 +279,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           sbuf ^= 1;
         }
-        buf ^= 1;
-        if (buf == 0) acc_ph ^= 1u;
-        continue;
-      }
+      } else {
 #pragma unroll 1
-      for (int c = 0; c < C::kBN / 32; ++c) {
-        uint32_t g[32], u[32];
-        tmem_ld_x32(tacc + c * 32, g);
-        tmem_ld_x32(tacc + C::kBN + c * 32, u);
-        tmem_wait_ld();
-        reg_fence(g);
-        reg_fence(u);
-        if (c == C::kBN / 32 - 1) {  // this CTA's half of the accumulator is read
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(tempty0_lead + 8u * buf);
-        }
-        if (lane == 0) bulk_wait_read<1>();
-        __syncwarp();
-        const uint32_t stg = sStg + (ew * 2 + sbuf) * C::kStgBytes;
-        const uint32_t row_addr = stg + lane * 64;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i0 = 8 * j + 2 * e;
-            w[e] = pack_bf16x2(
-                silu_mul(sg * __uint_as_float(g[i0]), su * __uint_as_float(u[i0])),
-                silu_mul(sg * __uint_as_float(g[i0 + 1]), su * __uint_as_float(u[i0 + 1])));
+        for (int c = 0; c < C::kBN / 32; ++c) {
+          uint32_t g[32], u[32];
+          tmem_ld_x32(tacc + c * 32, g);
+          tmem_ld_x32(tacc + C::kBN + c * 32, u);
+          tmem_wait_ld();
+          reg_fence(g);
+          reg_fence(u);
+          if (c == C::kBN / 32 - 1) {  // this CTA's half of the accumulator is read
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty0_lead + 8u * buf);
           }
-          st_shared_v4(row_addr + ((j ^ ((lane >> 1) & 3)) << 4), w[0], w[1], w[2], w[3]);
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+          const uint32_t stg = sStg + (ew * 2 + sbuf) * C::kStgBytes;
+          const uint32_t row_addr = stg + lane * 64;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int i0 = 8 * j + 2 * e;
+              w[e] = pack_bf16x2(
+                  silu_mul(sg * __uint_as_float(g[i0]), su * __uint_as_float(u[i0])),
+                  silu_mul(sg * __uint_as_float(g[i0 + 1]), su * __uint_as_float(u[i0 + 1])));
+            }
+            st_shared_v4(row_addr + ((j ^ ((lane >> 1) & 3)) << 4), w[0], w[1], w[2], w[3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int ncol = col0 + c * 32;
+            if (ncol < p.N && row0 < p.M) tma_store_2d(&p.tmap_y, stg, ncol, row0);
+            bulk_commit();
+          }
+          sbuf ^= 1;
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          const int ncol = col0 + c * 32;
-          if (ncol < p.N && row0 < p.M) tma_store_2d(&p.tmap_y, stg, ncol, row0);
-          bulk_commit();
-        }
-        sbuf ^= 1;
       }
       buf ^= 1;
       if (buf == 0) acc_ph ^= 1u;

@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
-  pdl_wait();  // the set-up above overlaps the previous grid; memory traffic starts here
+  pdl_wait();  // the set-up and L2 staging above overlap the previous grid; loads start here
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer -----
