@@ -62,13 +62,17 @@ def pack_reference(w1_bits: np.ndarray, w2_bits: np.ndarray, slice_k: int = PACK
     return out
 
 
-def unpack_reference(packed: np.ndarray, k_dim: int, n_dim: int):
-    """Inverse of ``pack_reference``: (W1, W2) as [K, N] uint16 arrays."""
+def unpack_reference(packed: np.ndarray, k_dim: int, n_dim: int, slice_k: int = PACK_BLOCK_K):
+    """Inverse of ``pack_reference`` with the same ``slice_k``: (W1, W2) as [K, N] arrays.
+
+    The element type is kept (uint16 bf16 bits for slice_k = 64, uint8 E4M3
+    bits for slice_k = 128).
+    """
+    p = np.asarray(packed)
     n_blocks = padded_n(n_dim) // PACK_BLOCK_N
-    k_slices = padded_k(k_dim) // PACK_BLOCK_K
-    p = np.asarray(packed, dtype=np.uint16).reshape(n_blocks, k_slices, 2 * PACK_BLOCK_N,
-                                                    PACK_BLOCK_K)
-    # [j, b, i, t] -> column 128 j + i, row 64 b + t
-    gate = p[:, :, :PACK_BLOCK_N, :].transpose(1, 3, 0, 2).reshape(k_slices * PACK_BLOCK_K, -1)
-    up = p[:, :, PACK_BLOCK_N:, :].transpose(1, 3, 0, 2).reshape(k_slices * PACK_BLOCK_K, -1)
+    k_slices = -(-k_dim // slice_k)
+    p = p.reshape(n_blocks, k_slices, 2 * PACK_BLOCK_N, slice_k)
+    # [j, b, i, t] -> column 128 j + i, row slice_k * b + t
+    gate = p[:, :, :PACK_BLOCK_N, :].transpose(1, 3, 0, 2).reshape(k_slices * slice_k, -1)
+    up = p[:, :, PACK_BLOCK_N:, :].transpose(1, 3, 0, 2).reshape(k_slices * slice_k, -1)
     return (np.ascontiguousarray(gate[:k_dim, :n_dim]), np.ascontiguousarray(up[:k_dim, :n_dim]))

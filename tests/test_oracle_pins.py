@@ -262,6 +262,70 @@ def test_tolerance_rule_boundaries():
     assert compare.mismatch_rate(y_bad, ref) == 1.0
 
 
+def test_relative_mismatch_rate_hand_values():
+    # the pages' accuracy figure: share of outputs more than 1 % from the
+    # reference, read over |ref| >= 1e-3 (the floor is included, ref = 0 is not)
+    bf = lambda v: f64_to_bf16_bits(np.array(v, dtype=np.float64))
+    # |ref| = 1e-3 exactly is compared (y = 0 is 100 % off); 0.99e-3 and 0 are not
+    ref = np.array([1e-3, 0.99e-3, 0.0, 0.5])
+    assert compare.relative_mismatch_rate(bf([0.0, 0.0, 0.25, 0.5]), ref) == 0.5
+    # the denominator is |ref|, not |y|: d = 0.00995 is 1.005 % of 0.99005 but
+    # 0.995 % of y = 1; the sign does not matter
+    assert compare.relative_mismatch_rate(bf([1.0]), np.array([0.99005])) == 1.0
+    assert compare.relative_mismatch_rate(bf([-1.0]), np.array([-0.99005])) == 1.0
+    # just under and just over 1 % (y exact in bf16): 2^-7 / (1 - 2^-7) = 0.787 %,
+    # 3 * 2^-8 / (1 - 3 * 2^-8) = 1.186 %
+    assert compare.relative_mismatch_rate(bf([1.0]), np.array([1.0 - 2.0 ** -7])) == 0.0
+    assert compare.relative_mismatch_rate(bf([1.0]), np.array([1.0 - 3 * 2.0 ** -8])) == 1.0
+    # the rate is over the compared elements only: 1 of 4 compared, 4 ignored
+    ref = np.array([1.0, 1.0, 1.0, 1.0, 1e-4, -1e-4, 0.0, 5e-4])
+    y = bf([1.0, 1.0, 1.0, 2.0, 1.0, 1.0, 1.0, 1.0])
+    assert compare.relative_mismatch_rate(y, ref) == 0.25
+    # nothing compared: 0, not NaN
+    assert compare.relative_mismatch_rate(bf([1.0, -1.0]), np.array([0.0, 1e-5])) == 0.0
+    assert compare.relative_mismatch_rate(bf([]), np.array([])) == 0.0
+
+
+def test_report_fields_on_hand_values():
+    # y as raw bf16 bits against a float64 reference, every field worked by hand
+    y = np.array([0x3F80,   # 1.0 against 1.0: exact
+                  0x3F81,   # 1.0078125 against 1.0: one bf16 step, within tolerance
+                  0x8001,   # -2^-133 against +0: one step across the signed zeros
+                  0x0002,   # 2 * 2^-133 against -2^-133 (bf16 0x8001)
+                  0x4000],  # 2.0 against 1.0: outside tolerance, 128 steps
+                 dtype=np.uint16)
+    tiny = 2.0 ** -133
+    ref = np.array([1.0, 1.0, 0.0, -tiny, 1.0])
+    rep = compare.report(y, ref)
+    assert rep["n"] == 5
+    assert rep["max_abs_err"] == 1.0
+    assert rep["max_excess"] == 1.0 - (1e-2 * 1.0 + 1e-3)
+    assert rep["tolerance_pass"] is False
+    assert rep["tolerance_pass"] == bool(compare.within_tolerance(y, ref).all())
+    assert rep["mismatch_rate"] == pytest.approx(0.2, abs=1e-15)
+    assert rep["relative_mismatch_rate"] == 1.0 / 3.0       # |ref| >= 1e-3: three, one off
+    # steps: 0, 1, 1 (0x8001 vs +0), 3 (0x0002 vs 0x8001 = -1 on the ordered line), 128
+    assert compare.bf16_ulp_distance(y, ref).tolist() == [0, 1, 1, 3, 128]
+    assert rep["max_bf16_ulp"] == 128
+    assert rep["bf16_ulp_gt1_rate"] == pytest.approx(0.4, abs=1e-15)
+    assert rep["nonfinite"] == 0
+    # dropping the failing element passes
+    assert compare.report(y[:4], ref[:4])["tolerance_pass"] is True
+
+
+def test_report_counts_non_finite_outputs_and_fails_them():
+    y = np.array([0x7FC0, 0x7F80, 0xFF80, 0x3F80, 0xFFC1], dtype=np.uint16)  # NaN, +inf, -inf, 1, NaN
+    ref = np.ones(5)
+    rep = compare.report(y, ref)
+    assert rep["nonfinite"] == 4
+    assert rep["tolerance_pass"] is False
+    assert compare.within_tolerance(y, ref).tolist() == [False, False, False, True, False]
+    assert rep["mismatch_rate"] == pytest.approx(0.8, abs=1e-15)
+    # an empty comparison passes vacuously and reports zeros
+    empty = compare.report(np.zeros(0, dtype=np.uint16), np.zeros(0))
+    assert empty["n"] == 0 and empty["tolerance_pass"] and empty["max_bf16_ulp"] == 0
+
+
 # ------------------------------------------------------ packed layout ----
 
 def test_pack_layout_indices_and_padding():
@@ -363,6 +427,18 @@ def test_fp8_pack_layout_uses_128_value_slices():
             b, t = divmod(k, 128)
             assert p[j, b, i, t] == w1[k, n] and p[j, b, 128 + i, t] == w2[k, n]
     assert not p[1, :, 8:128].any() and not p[:, 1, :, 72:].any()
+
+
+def test_fp8_pack_layout_round_trip():
+    rng = np.random.default_rng(6)
+    w1 = rng.integers(0, 256, size=(144, 264), dtype=np.uint8)
+    w2 = rng.integers(0, 256, size=(144, 264), dtype=np.uint8)
+    p = pack_layout.pack_reference(w1, w2, slice_k=128)
+    u1, u2 = pack_layout.unpack_reference(p, 144, 264, slice_k=128)
+    assert u1.dtype == np.uint8 and np.array_equal(u1, w1) and np.array_equal(u2, w2)
+    # the bf16 slicing does not invert the FP8 layout
+    with pytest.raises(ValueError):
+        pack_layout.unpack_reference(p, 144, 264)
 
 
 # ----------------------------------------------------- down-projection ----
