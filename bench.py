@@ -1,23 +1,28 @@
 """Benchmark of the fused SwiGLU projection Y = SiLU(A W1) * (A W2) on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--impl ours|reference] [--no-cpu-baseline]
+                    [--secondary NAMES] [--impl ours|reference] [--no-cpu-baseline]
 
 One step = one swiglu_forward call over one batch of synthetic input (the
 packed weight is prepared once, before timing, as at model load). Prints one
-JSON line (rank 0). Metric: TFLOP/s counted as 4*M*K*N per step.
+JSON line (rank 0). Metric: TFLOP/s counted as 4*M*K*N per step, and its
+fraction of the dense BF16 tensor peak. Default workload: the Qwen-2.5-72B
+MLP gate/up projection on 8192 tokens (M=8192, K=8192, N=29568), the largest
+prefill shape; the 7B decode batch (M=16) follows as a secondary record.
 
 * value: whole-job TFLOP/s with inputs resident in HBM; K steps timed with
-  CUDA events between barriers + synchronisations, max over ranks. The steps
-  replay from CUDA graphs captured from swiglu_forward calls (--eager: one
-  host call per step).
-* roofline: the fused kernel's achieved bytes/s (decode workloads, HBM bound)
-  or FLOP/s (prefill workloads, tensor bound) per launch (timed region over
-  launches: one launch per step), against the measured peaks in
-  MEASURED_PEAKS.json.
+  CUDA events between barriers + synchronisations, max over ranks. The K steps
+  replay from one CUDA graph of exactly K kernel nodes captured from
+  swiglu_forward calls (longer runs: whole-rotation graphs plus a remainder
+  graph; --eager: one host call per step).
+* roofline: the fused kernel's achieved bytes/s (HBM-bound workloads) or
+  FLOP/s (tensor-bound workloads) per launch (timed region over launches: one
+  launch per step), against the measured peaks in MEASURED_PEAKS.json.
 * e2e: the same metric through swiglu_forward_from_host, with each step's
   activations copied from pinned host memory and its output copied back;
   alternate steps go to two streams with their own staging buffers.
+* secondary: other workloads through the same device-timed path (value,
+  roofline, clocks), one record each.
 * cpu_baseline: the CPU oracle (float64) on a bounded sample of the workload.
 * --impl reference: the CPU oracle timed as the reference arm (the method has
   no runnable reference implementation).
@@ -51,11 +56,15 @@ sys.path.insert(0, ROOT)
 
 from swiglu_gated_mlp_gb300.workloads import (WORKLOADS, Workload, bf16_bits,  # noqa: E402
                                               make_inputs, make_inputs_fp8, make_workload_inputs,
-                                              sweep_32b)
+                                              sample_rows, sweep_32b)
 
 METRIC = "fused SwiGLU-GEMM TFLOP/s (4·M·K·N) and % of GB300 dense BF16 peak"
 METRIC_DOWN = "MLP down-projection TFLOP/s (2·M·N·H), Out = Y·W3 + R"
-DEFAULT_WORKLOAD = "qwen2.5-7b-decode-m16"
+# the metric is a fraction of the dense BF16 tensor peak: its headline is the
+# largest prefill shape (Qwen-2.5-72B, 8192 tokens); the 7B decode batch, the
+# HBM-bound case, is reported beside it as a secondary record
+DEFAULT_WORKLOAD = "qwen2.5-72b-prefill-m8192"
+DEFAULT_SECONDARY = "qwen2.5-7b-decode-m16"
 # swiglu_forward_variant's kernel choice (auto = what swiglu_forward does)
 VARIANTS = {"auto": 0, "large": 1, "small": 2, "pair": 3, "sequential": 4}
 L2_BYTES = 129 * 1024 * 1024
@@ -219,13 +228,32 @@ class ClockSampler:
 
 # ------------------------------------------------------------- our arm ----
 
-def run_ours(args, w: Workload, world: int, rank: int, local: int):
-    import swiglu_gated_mlp_gb300 as sg
-    from swiglu_gated_mlp_gb300 import build as _build
-    _build.build_library()
-    dev = torch.device("cuda", torch.cuda.current_device())
-    M, K, N = w.M, w.K, w.N
+@dataclasses.dataclass
+class Prepared:
+    """One workload on the device: rotating operand copies and the forward call."""
+    w: Workload
+    fp8: bool
+    down: bool
+    flops: int
+    alg_bytes: int
+    copies: int
+    plan: str
+    kernel: str
+    fwd: object            # fwd(j, stream=None): one forward on rotation slot j
+    out_cols: int
+    w_bytes: int
+    a_cpu: object          # the step's activations (CPU), for the e2e leg
+    host: dict             # CPU inputs kept for the oracle legs
+    dev_state: dict        # device tensors (dropped by release())
 
+    def release(self):
+        self.dev_state.clear()
+        self.fwd = None
+
+
+def prepare(args, sg, w: Workload, dev) -> Prepared:
+    """Inputs, packed weights and rotating copies for workload `w` on `dev`."""
+    M, K, N = w.M, w.K, w.N
     fp8 = args.dtype == "fp8"
     down = args.op == "down"
     if down and fp8:
@@ -233,6 +261,7 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     elem = 1 if fp8 else 2
     flops = w.flops
     alg_bytes = elem * M * K + 2 * elem * K * N + 2 * M * N  # A, W1 and W2 once, Y (bf16)
+    host = {}
     if down:
         # Out [M, H] = Y [M, N] x W3 [N, H] + R at this workload's MLP shape (H = K)
         H = K
@@ -243,11 +272,12 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
         wp0 = sg.swiglu_pack_down_weights(w3_cpu.to(dev))
         a_cpu = y_cpu
     elif fp8:
-        a_cpu, w1_cpu, w2_cpu, (s_a, s_1, s_2) = make_inputs_fp8(M, K, N, w.seed)
+        a_cpu, w1_cpu, w2_cpu, scales = make_inputs_fp8(M, K, N, w.seed)
         wp0 = sg.swiglu_pack_weights_fp8(w1_cpu.to(dev), w2_cpu.to(dev))
     else:
         a_cpu, w1_cpu, w2_cpu = make_workload_inputs(w)
         wp0 = sg.swiglu_pack_weights(w1_cpu.to(dev), w2_cpu.to(dev))
+        host.update(a=a_cpu, w1=w1_cpu, w2=w2_cpu)
     torch.cuda.synchronize()
     w_bytes = wp0.numel() * wp0.element_size()
     # Inputs larger than L2 between consecutive steps: rotate copies of the
@@ -266,6 +296,7 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     As = [a0] + [a0.clone() for _ in range(copies - 1)]
     out_cols = K if down else N
     Ys = [torch.empty(M, out_cols, dtype=torch.bfloat16, device=dev) for _ in range(copies)]
+    Rs = None
     if down:
         r0 = r_cpu.to(dev)
         Rs = [r0] + [r0.clone() for _ in range(copies - 1)]
@@ -273,47 +304,73 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     plan = (sg.swiglu_down_plan_string(M, N, K) if down else
             sg.swiglu_plan_string_fp8(M, K, N) if fp8 else
             sg.swiglu_plan_string(M, K, N, variant))
-    stream = torch.cuda.current_stream(dev)
+    base = plan.split(" ", 1)[1] if plan.startswith(("down ", "fp8 ")) else plan
+    kernel = ("fused_small_m_kernel" if base.startswith("small_m") else
+              "fused_large_m_pair_kernel" if base.startswith("large_m_pair") else
+              "fused_sequential_kernel" if base.startswith("sequential") else
+              "fused_large_m_kernel")
+    if down or fp8:  # the template instance: <fp8> is E4M3 inputs, <down> the down-projection
+        kernel += "<down>" if down else "<fp8>"
 
     def fwd(j, s=None):
         """One forward on rotation slot j (on stream s, default the current stream)."""
         if down:
             sg.swiglu_down_forward(As[j], wps[j], K, R=Rs[j], Out=Ys[j], stream=s)
         elif fp8:
-            sg.swiglu_forward_fp8(As[j], wps[j], N, s_a, s_1, s_2, Y=Ys[j], stream=s)
+            sg.swiglu_forward_fp8(As[j], wps[j], N, *scales, Y=Ys[j], stream=s)
         else:
             sg.swiglu_forward_variant(As[j], wps[j], N, variant, Y=Ys[j], stream=s)
 
+    if fp8:
+        host["scales"] = scales
+    return Prepared(w=w, fp8=fp8, down=down, flops=flops, alg_bytes=alg_bytes, copies=copies,
+                    plan=plan, kernel=kernel, fwd=fwd, out_cols=out_cols, w_bytes=w_bytes,
+                    a_cpu=a_cpu, host=host,
+                    dev_state={"wps": wps, "As": As, "Ys": Ys, "Rs": Rs})
+
+
+def time_steps(args, sg, pr: Prepared, steps: int, world: int, dev, stream):
+    """W eager warm-up steps, then exactly `steps` steps timed with CUDA events.
+
+    Returns (steps, seconds on this rank, max over ranks, launch note, clocks).
+    """
+    copies = pr.copies
+
     def step(i):
-        fwd(i % copies, stream)
+        pr.fwd(i % copies, stream)
 
     for i in range(args.warmup):
         step(i)
     sg.swiglu_check_device_status(stream=stream)
 
-    # Steps replay from CUDA graphs (one kernel node per step, captured from the
-    # same swiglu_forward calls), so the host's per-call cost does not pace
-    # microsecond-scale launches; the e2e leg below keeps per-call launches.
-    run_steps, graph_note = eager_runner(step), "eager launches"
-    if not args.eager:
-        try:
-            run_steps = graph_runner(fwd, copies, stream)
-            graph_note = (f"CUDA graph replay: graphs of {run_steps.block_steps} steps "
-                          f"(turns of the {copies}-slot rotation) and single-step graphs for "
-                          f"the remainder; one kernel node per step")
-        except Exception as exc:  # capture refused: keep eager launches, say so
-            graph_note = f"eager launches (graph capture failed: {type(exc).__name__})"
-            torch.cuda.synchronize()
-    run_steps(2 * copies)
-    torch.cuda.synchronize()
-
-    steps = args.steps
     if steps <= 0:  # auto: about two seconds of timed work
+        for i in range(2 * copies):
+            step(i)
+        torch.cuda.synchronize()
         t0 = time.perf_counter()
-        run_steps(4 * copies)
+        for i in range(4 * copies):
+            step(i)
         torch.cuda.synchronize()
         est = (time.perf_counter() - t0) / (4 * copies)
         steps = int(min(max(50, 2.0 / max(est, 1e-6)), 200000))
+
+    # The timed steps replay from CUDA graphs captured from the same forward
+    # calls (one kernel node per step), so consecutive launches overlap through
+    # programmatic dependent launch as they do in a model's step, and the
+    # host's per-call cost does not pace microsecond-scale kernels.
+    run_steps, note = eager_runner(step), "eager launches, one host call per step"
+    if not args.eager:
+        try:
+            run_steps = graph_runner(pr.fwd, copies, stream, steps)
+            note = (f"CUDA graph replay of exactly {steps} steps: "
+                    f"{run_steps.block_replays} replay(s) of a {run_steps.block_steps}-step graph"
+                    + (f" + one {run_steps.tail_steps}-step graph" if run_steps.tail_steps else "")
+                    + "; one kernel node per step, steps rotate over the operand copies")
+        except Exception as exc:  # capture refused: keep eager launches, say so
+            note = f"eager launches (graph capture failed: {type(exc).__name__})"
+            torch.cuda.synchronize()
+    run_steps.warm() if hasattr(run_steps, "warm") else run_steps(min(steps, 2 * copies))
+    torch.cuda.synchronize()
 
     t_begin = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
@@ -328,48 +385,72 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     barrier(world)
     sg.swiglu_check_device_status(stream=stream)
     elapsed = t_begin.elapsed_time(t_end) * 1e-3
-    elapsed_max = max_over_ranks(elapsed, world)
-    value = aggregate(flops, steps, elapsed_max, world)
+    return steps, elapsed, max_over_ranks(elapsed, world), note, sampler.summary()
+
+
+def roofline(pr: Prepared, avg_launch: float, peaks: dict, peak_src: str) -> dict:
+    """The fused kernel's achieved rate per launch against the measured peaks."""
+    # FP8 tensor peak: the measured bf16 figures times the nominal fp8/bf16
+    # ratio (4.5 / 2.25 PFLOP/s dense).
+    tensor_peak = peaks["bf16_tflops"] * (2.0 if pr.fp8 else 1.0)
+    tensor_sus = peaks.get("bf16_tflops_sustained")
+    tensor_sus = tensor_sus * (2.0 if pr.fp8 else 1.0) if tensor_sus else None
+    hbm_bound = pr.flops / pr.alg_bytes < tensor_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    traffic, traffic_src = profiled_traffic(pr.kernel, pr.w.name)
+    if hbm_bound:
+        achieved = pr.alg_bytes / avg_launch / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": traffic, "algorithmic_bytes": pr.alg_bytes}
+    else:
+        achieved = pr.flops / avg_launch / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(tensor_peak, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / tensor_peak, 4),
+                "traffic": traffic, "algorithmic_flops": pr.flops,
+                "algorithmic_bytes": pr.alg_bytes,
+                "peak_sustained": round(tensor_sus, 1) if tensor_sus else None,
+                "frac_sustained": round(achieved / tensor_sus, 4) if tensor_sus else None}
+    roof.update({"kernel": pr.kernel, "plan": pr.plan, "avg_launch_us": round(avg_launch * 1e6, 3),
+                 "peak_source": peak_src + (
+                     ", copy bandwidth" if hbm_bound else
+                     ", bf16 burst x 2 (nominal fp8/bf16 ratio)" if pr.fp8 else ", burst"),
+                 "traffic_source": traffic_src})
+    return roof
+
+
+def l2_note(pr: Prepared) -> str:
+    return (f"inputs larger than L2: {pr.copies} rotating copies of "
+            f"{'Y, packed W3, R and Out' if pr.down else 'A, packed W and Y'} "
+            f"({pr.copies * pr.alg_bytes / 2**20:.0f} MiB; "
+            f"{(pr.copies - 1) * pr.alg_bytes / 2**20:.0f} MiB of other copies "
+            f"between two uses of one)")
+
+
+def run_ours(args, w: Workload, world: int, rank: int, local: int):
+    import swiglu_gated_mlp_gb300 as sg
+    from swiglu_gated_mlp_gb300 import build as _build
+    _build.build_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream(dev)
+    M, K, N = w.M, w.K, w.N
+    peaks, peak_src = load_peaks()
+
+    pr = prepare(args, sg, w, dev)
+    fp8, down, out_cols = pr.fp8, pr.down, pr.out_cols
+    steps, elapsed, elapsed_max, graph_note, clocks = time_steps(args, sg, pr, args.steps, world,
+                                                                 dev, stream)
+    value = aggregate(pr.flops, steps, elapsed_max, world)
     # One fused-kernel launch per step and nothing else in the timed region, so
     # the average launch duration is the region's CUDA-event time over the
     # launches (events between launches would block the launch overlap).
     avg_launch = elapsed / steps
-
-    peaks, peak_src = load_peaks()
-    # FP8 tensor peak: the measured bf16 figures times the nominal fp8/bf16
-    # ratio (4.5 / 2.25 PFLOP/s dense).
-    tensor_peak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
-    tensor_sus = peaks.get("bf16_tflops_sustained")
-    tensor_sus = tensor_sus * (2.0 if fp8 else 1.0) if tensor_sus else None
-    hbm_bound = flops / alg_bytes < tensor_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    base = plan.split(" ", 1)[1] if plan.startswith(("down ", "fp8 ")) else plan
-    kernel = ("fused_small_m_kernel" if base.startswith("small_m") else
-              "fused_large_m_pair_kernel" if base.startswith("large_m_pair") else
-              "fused_sequential_kernel" if base.startswith("sequential") else
-              "fused_large_m_kernel")
-    if down or fp8:  # the template instance: <fp8> is E4M3 inputs, <down> the down-projection
-        kernel += "<down>" if down else "<fp8>"
-    traffic, traffic_src = profiled_traffic(kernel, w.name)
-    if hbm_bound:
-        achieved = alg_bytes / avg_launch / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": traffic, "algorithmic_bytes": alg_bytes}
-    else:
-        achieved = flops / avg_launch / 1e12
-        sus = tensor_sus
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(tensor_peak, 1),
-                "unit": "TFLOP/s", "frac": round(achieved / tensor_peak, 4),
-                "traffic": traffic, "algorithmic_flops": flops,
-                "peak_sustained": round(sus, 1) if sus else None,
-                "frac_sustained": round(achieved / sus, 4) if sus else None}
-    roof.update({"kernel": kernel, "plan": plan, "avg_launch_us": round(avg_launch * 1e6, 3),
-                 "peak_source": peak_src + (
-                     ", copy bandwidth" if hbm_bound else
-                     ", bf16 burst x 2 (nominal fp8/bf16 ratio)" if fp8 else ", burst"),
-                 "traffic_source": traffic_src})
+    roof = roofline(pr, avg_launch, peaks, peak_src)
 
     # ---- end to end through the public API: host activations in, host output out
+    a_cpu = pr.a_cpu
+    wps = pr.dev_state["wps"]
+    Rs = pr.dev_state["Rs"]
+    copies = pr.copies
     a_host = [a_cpu.pin_memory()] + [a_cpu.clone().pin_memory() for _ in range(min(copies, 4) - 1)]
     y_host = [torch.empty(M, out_cols, dtype=torch.bfloat16).pin_memory()
               for _ in range(len(a_host))]
@@ -394,8 +475,8 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
         elif fp8:  # host copies through torch around the FP8 call
             with torch.cuda.stream(st):
                 a_dev[b].copy_(a_host[j], non_blocking=True)
-                sg.swiglu_forward_fp8(a_dev[b], wps[i % copies], N, s_a, s_1, s_2, Y=y_dev[b],
-                                      stream=st)
+                sg.swiglu_forward_fp8(a_dev[b], wps[i % copies], N, *pr.host["scales"],
+                                      Y=y_dev[b], stream=st)
                 y_host[j].copy_(y_dev[b], non_blocking=True)
         else:
             sg.swiglu_forward_from_host(a_host[j], wps[i % copies], N, y_host[j], a_dev[b],
@@ -412,14 +493,16 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
     barrier(world)
     sg.swiglu_check_device_status(stream=stream)
-    e2e = {"value": round(aggregate(flops, e2e_steps, e2e_s, world), 3), "unit": "TFLOP/s",
+    e2e = {"value": round(aggregate(pr.flops, e2e_steps, e2e_s, world), 3), "unit": "TFLOP/s",
            "h2d_bytes_per_step": a_cpu.numel() * a_cpu.element_size(),
            "d2h_bytes_per_step": 2 * M * out_cols,
            "steps": e2e_steps, "streams": len(e2e_streams),
            "api": ("pinned-host copies + swiglu_down_forward" if down else
                    "pinned-host copies + swiglu_forward_fp8" if fp8 else
                    "swiglu_forward_from_host")}
+    del a_dev, y_dev, a_host, y_host, wps, Rs, e2e_step
 
+    tensor_peak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
     out = {
         "metric": METRIC_DOWN if down else METRIC, "value": round(value, 3), "unit": "TFLOP/s",
         "n_gpus": world,
@@ -431,11 +514,7 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
                    "variant": args.variant, "inputs": args.dtype, "op": args.op,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "launch": graph_note,
-                   "l2": f"inputs larger than L2: {copies} rotating copies of "
-                         f"{'Y, packed W3, R and Out' if down else 'A, packed W and Y'} "
-                         f"({copies * alg_bytes / 2**20:.0f} MiB; "
-                         f"{(copies - 1) * alg_bytes / 2**20:.0f} MiB of other copies "
-                         f"between two uses of one)",
+                   "l2": l2_note(pr),
                    "note": (f"down-projection Out[M,H] = Y[M,N] W3[N,H] + R at this workload's "
                             f"MLP shape, H = {K}" if down else w.note)},
         "pct_bf16_peak": round(100 * value / world / peaks["bf16_tflops"], 3),
@@ -443,17 +522,47 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
         "roofline": roof,
         "e2e": e2e,
         "gpu_launches": steps,
-        "clocks": sampler.summary(),
-        "packed_weight_bytes": w_bytes,
+        "clocks": clocks,
+        "packed_weight_bytes": pr.w_bytes,
     }
-    if args.compare_unfused and not fp8:
-        out["unfused"] = unfused_comparison(w, As, w1_cpu.to(dev), w2_cpu.to(dev), copies, steps,
-                                            elapsed / steps, peaks)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if args.compare_unfused and not (fp8 or down):
+        out["unfused"] = unfused_comparison(w, pr.dev_state["As"], pr.host["w1"].to(dev),
+                                            pr.host["w2"].to(dev), copies, steps, elapsed / steps,
+                                            peaks)
+    y_check = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not (down or fp8):
         # the timed output itself (every rotation slot holds the same inputs) is
         # compared with the oracle values the baseline computes anyway
-        y_check = None if (down or fp8) else bf16_bits(Ys[0].cpu())
-        out["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds, y_gpu_bits=y_check)
+        y_check = bf16_bits(pr.dev_state["Ys"][0].cpu())
+    host = pr.host
+    pr.release()
+    del pr
+    torch.cuda.empty_cache()
+
+    # ---- secondary records: other workloads, same timing path, device-timed only
+    secondary = []
+    if args.secondary and not (down or fp8 or args.m or args.variant != "auto"):
+        for name in [s for s in args.secondary.split(",") if s and s != w.name]:
+            ws = workload_by_name(name)
+            ps = prepare(args, sg, ws, dev)
+            s_steps, s_el, s_max, s_note, s_clocks = time_steps(args, sg, ps, args.steps, world,
+                                                                dev, stream)
+            secondary.append({
+                "workload": ws.name, "M": ws.M, "K": ws.K, "N": ws.N, "seed": ws.seed,
+                "value": round(aggregate(ps.flops, s_steps, s_max, world), 3), "unit": "TFLOP/s",
+                "steps": s_steps, "ms_per_step": round(s_max / s_steps * 1e3, 6),
+                "gpu_launches": s_steps, "launch": s_note, "l2": l2_note(ps),
+                "roofline": roofline(ps, s_el / s_steps, peaks, peak_src), "clocks": s_clocks,
+                "note": ws.note})
+            ps.release()
+            del ps
+            torch.cuda.empty_cache()
+    if secondary:
+        out["secondary"] = secondary
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not (down or fp8):
+        out["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds, y_gpu_bits=y_check,
+                                           inputs=(host["a"], host["w1"], host["w2"]))
     return out
 
 
@@ -466,36 +575,52 @@ def eager_runner(step):
     return run
 
 
-def graph_runner(fwd, copies, stream, min_block=64):
-    """Captures the fused forward into CUDA graphs.
+def graph_runner(fwd, copies, stream, steps, max_block=512):
+    """Captures exactly `steps` forward steps into CUDA graphs.
 
-    One graph holds `block` consecutive steps (whole turns of the rotation, at
-    least `min_block` steps, so consecutive kernels inside it overlap their
-    launches), and single-step graphs cover a remainder.
+    Up to `max_block` steps: one graph of exactly `steps` kernel nodes, so the
+    whole timed region is one replay and every launch after the first overlaps
+    its predecessor. More steps: a graph of whole turns of the rotation
+    (about 256 steps), replayed, plus one graph of the remainder; both start at
+    rotation slot 0, so slots keep their order across replays.
     """
-    block_steps = copies * max(1, -(-min_block // copies))
+    if steps <= max_block:
+        block_steps, tail_steps = steps, 0
+    else:
+        block_steps = copies * max(1, 256 // copies)
+        tail_steps = steps % block_steps
+    replays = steps // block_steps
     side = torch.cuda.Stream(stream.device)
     side.wait_stream(stream)
-    block = torch.cuda.CUDAGraph()
-    singles = []
+    graphs = []
     with torch.cuda.stream(side):
-        with torch.cuda.graph(block, stream=side):
-            for i in range(block_steps):
-                fwd(i % copies)
-        for j in range(copies):
+        for n in (block_steps, tail_steps):
+            if n == 0:
+                graphs.append(None)
+                continue
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=side):
-                fwd(j)
-            singles.append(g)
+                for i in range(n):
+                    fwd(i % copies)
+            graphs.append(g)
     stream.wait_stream(side)
     torch.cuda.synchronize()
+    block, tail = graphs
 
     def run(n):
-        for _ in range(n // block_steps):
+        assert n == steps, "the graphs hold exactly the timed step count"
+        for _ in range(replays):
             block.replay()
-        for i in range(n % block_steps):
-            singles[i % copies].replay()
-    run.block_steps = block_steps
+        if tail is not None:
+            tail.replay()
+
+    def warm():
+        # first replays upload the graphs; not part of the timed region
+        block.replay()
+        if tail is not None:
+            tail.replay()
+
+    run.block_steps, run.tail_steps, run.block_replays, run.warm = block_steps, tail_steps, replays, warm
     return run
 
 
@@ -562,25 +687,29 @@ def _oracle_sample_call(a_bits, w1_bits, w2_bits, cols):
     return swiglu_f64(a_bits, w1_bits[:, cols], w2_bits[:, cols])
 
 
-def cpu_baseline(w: Workload, budget_s: float = 12.0, per_step_s: float | None = None,
-                 y_gpu_bits=None):
-    """The float64 CPU oracle, as it stands, on a bounded column sample of the workload.
+def cpu_baseline(w: Workload, budget_s: float = 12.0, y_gpu_bits=None, inputs=None,
+                 max_rows: int = 512):
+    """The float64 CPU oracle, as it stands, on a bounded sample of the workload.
 
-    Rows are kept whole; a contiguous block of output columns is taken so that
-    one call costs about `per_step_s` (or the whole budget is split into
-    several calls). Returns TFLOP/s counted like the GPU metric (4*M*K*cols).
+    Up to `max_rows` rows are kept (all of them for small M; else a seeded
+    subset that includes rows 0 and M-1), and a contiguous block of output
+    columns is taken so that one call costs about a quarter of the budget.
+    Returns TFLOP/s counted like the GPU metric (4 * rows * K * cols per
+    call) and the time a whole step would take at that rate (extrapolated).
     With `y_gpu_bits` (the GPU's Y as bf16 bits), the oracle values of every
     call are also compared with it, outside the timed calls ("parity").
     """
-    a, w1, w2 = make_workload_inputs(w)
-    a_bits, w1_bits, w2_bits = bf16_bits(a), bf16_bits(w1), bf16_bits(w2)
+    a, w1, w2 = inputs if inputs is not None else make_workload_inputs(w)
+    rows = sample_rows(w.M, max_rows, seed=w.seed)
+    a_bits = bf16_bits(a)[rows]
+    w1_bits, w2_bits = bf16_bits(w1), bf16_bits(w2)
     # calibrate on a small block
     probe_cols = max(8, min(w.N, 256))
     t0 = time.perf_counter()
     _oracle_sample_call(a_bits, w1_bits, w2_bits, slice(0, probe_cols))
     t_probe = max(time.perf_counter() - t0, 1e-4)
     per_col = t_probe / probe_cols
-    target = per_step_s if per_step_s else min(budget_s / 4, 3.0)
+    target = min(budget_s / 4, 3.0)
     cols = int(max(8, min(w.N, target / per_col)))
     calls, total_t, flops = 0, 0.0, 0
     checked = []  # (GPU bits, oracle values) per checked column block
@@ -591,18 +720,21 @@ def cpu_baseline(w: Workload, budget_s: float = 12.0, per_step_s: float | None =
         ref = _oracle_sample_call(a_bits, w1_bits, w2_bits, slice(c0, c0 + cols))
         total_t += time.perf_counter() - t0
         if y_gpu_bits is not None and calls < 4:
-            checked.append((y_gpu_bits[:, c0:c0 + cols], ref))
-        flops += 4 * w.M * w.K * cols
+            checked.append((y_gpu_bits[rows][:, c0:c0 + cols], ref))
+        flops += 4 * len(rows) * w.K * cols
         calls += 1
-        if per_step_s or time.perf_counter() - t_start > budget_s:
+        if time.perf_counter() - t_start > budget_s:
             break
-    out = {"value": round(flops / total_t / 1e12, 6), "unit": "TFLOP/s", "cores": _CORES,
+    rate = flops / total_t
+    row_text = (f"all {w.M} rows" if len(rows) == w.M else
+                f"{len(rows)} of {w.M} rows (seeded subset with rows 0 and {w.M - 1})")
+    out = {"value": round(rate / 1e12, 6), "unit": "TFLOP/s", "cores": _CORES,
            "kind": "oracle",
-           "sample": f"{calls} call(s) of the float64 oracle on all {w.M} rows x {cols} of "
+           "sample": f"{calls} call(s) of the float64 oracle on {row_text} x {cols} of "
                      f"{w.N} columns (K={w.K}), {total_t:.1f} s of CPU time",
+           "full_step_s_extrapolated": round(w.flops / rate, 1),
            "threads_env": os.environ.get("OPENBLAS_NUM_THREADS")}
     if checked:
-        import numpy as np
         from oracle import compare
         rep = compare.report(np.concatenate([c[0] for c in checked], axis=1),
                              np.concatenate([c[1] for c in checked], axis=1))
@@ -714,6 +846,9 @@ def main(argv=None):
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--secondary", default=DEFAULT_SECONDARY,
+                   help="comma-separated workloads timed after the main one, reported under "
+                        "'secondary' (device-timed value and roofline); '' for none")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--rotate", type=int, default=0,
                    help="rotating copies of the operands (0: enough that 32 x L2 bytes of "

@@ -87,7 +87,9 @@ typedef enum {
 } swiglu_variant_t;
 
 /*
- * Size in bytes of the packed weight for a K x N gate/up pair:
+ * Size in bytes of the packed weight for a K x N gate/up pair (infrastructure
+ * of the boundary: no passage of the pages defines it; it sizes the buffer
+ * swiglu_pack_weights fills):
  * 2 (matrices) * Np * Kp * 2 (bytes), Np = N rounded up to a multiple of 128,
  * Kp = K rounded up to a multiple of 64.
  * Returns 0 if K <= 0, N <= 0 or a size is beyond the limits below.
@@ -160,15 +162,17 @@ SWIGLU_API swiglu_status_t swiglu_forward_from_host(const void* A_host, const vo
                                                     swiglu_stream_t stream);
 
 /*
- * Synchronises `stream`, then reads and clears the current device's status
- * word. Returns SWIGLU_ERR_TIMEOUT if any kernel since the last check gave up
+ * Infrastructure of the boundary (no passage of the pages defines it: the
+ * pages describe no failure handling). Synchronises `stream`, then reads and
+ * clears the current device's status word. Returns SWIGLU_ERR_TIMEOUT if any kernel since the last check gave up
  * on a pipeline wait (every wait in the kernels is bounded; the kernel then
  * stops cleanly and releases its resources), SWIGLU_ERR_CUDA if the stream
  * reports an error, SWIGLU_OK otherwise.
  */
 SWIGLU_API swiglu_status_t swiglu_check_device_status(swiglu_stream_t stream);
 
-/* Static, human-readable name of a status code (never NULL). */
+/* Static, human-readable name of a status code (never NULL). Infrastructure of
+ * the boundary; no passage of the pages defines it. */
 SWIGLU_API const char* swiglu_status_string(swiglu_status_t status);
 
 /*
@@ -249,10 +253,10 @@ SWIGLU_API swiglu_status_t swiglu_down_plan_string(int64_t M, int64_t N, int64_t
                                                    size_t buflen);
 
 /*
- * Allocation-free forward for callers that cannot call cudaMalloc: code that
- * runs while a stream is being captured into a CUDA graph (allocation is not
- * allowed there), serving runtimes that reserve all device memory for their
- * own pools up front, and hosts that forbid allocation after start-up. The
+ * Allocation-free forward for callers that cannot call cudaMalloc: serving
+ * runtimes that reserve all device memory for their own pools up front (a
+ * library allocation would fail, or would fragment memory the runtime plans
+ * to the byte), and hosts that forbid allocation once start-up is over. The
  * other forward entry points allocate one small status record per device on
  * first use; this one runs the decode (small-M) kernel with that record in a
  * file-scope static device array of 256 bytes instead, held by every GPU that
@@ -260,13 +264,17 @@ SWIGLU_API swiglu_status_t swiglu_down_plan_string(int64_t M, int64_t N, int64_t
  * this is a deployment variant, not part of the method.
  *
  * Same arguments and result as swiglu_forward, for M <= 256 (larger M:
- * UNSUPPORTED). The caller passes every input and output; the library
- * allocates nothing (no cudaMalloc, cudaFree or allocating library call).
+ * UNSUPPORTED). The launch shape does not depend on the device: one CTA per
+ * 128-column block holding all M tokens (no K split over clusters, no token
+ * groups), so it can differ from swiglu_forward's for M > 32 or narrow N.
+ * The caller passes every input and output; the library allocates nothing
+ * (no cudaMalloc, cudaFree or allocating library call).
  * Each call clears the shared status record on `stream` before the kernel;
  * if `status_out` (HOST, 4 x uint32, may be NULL) is given, the record is
  * copied there after the kernel, on `stream`: status_out[0] is 0, or 4
  * (SWIGLU_ERR_TIMEOUT) if a pipeline wait gave up; read it after the stream
- * synchronises (page-locked memory keeps the copy asynchronous).
+ * synchronises (page-locked memory keeps the copy asynchronous; pageable
+ * memory makes the call wait for the kernel).
  * The first call on a device does a one-time set-up (kernel attributes and the
  * array's device address); make that first call before any stream capture.
  * Calls whose kernels overlap on the GPU (several streams) share the record

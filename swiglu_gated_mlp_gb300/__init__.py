@@ -5,11 +5,14 @@
 The public functions mirror the C ABI in include/swiglu.h (same names):
 ``swiglu_pack_weights``, ``swiglu_forward``, ``swiglu_forward_variant``,
 ``swiglu_forward_from_host``, ``swiglu_packed_weight_bytes``,
-``swiglu_check_device_status``, ``swiglu_status_string``, ``swiglu_plan_string``.
+``swiglu_check_device_status``, ``swiglu_status_string``, ``swiglu_plan_string``
+and the FP8, down-projection and allocation-free forms; ``pack(W1, W2)`` and
+``forward(A, Wp, N)`` are short names of the first two.
 They load the compiled library on first use and raise if it is missing; there
 is no CPU or PyTorch fallback.
 """
 _EXPORTS = {
+    "pack", "forward",
     "swiglu_pack_weights", "swiglu_forward", "swiglu_forward_variant", "swiglu_forward_from_host",
     "swiglu_forward_noalloc", "swiglu_pack_weights_fp8", "swiglu_forward_fp8",
     "swiglu_packed_weight_bytes_fp8", "swiglu_down_packed_bytes", "swiglu_pack_down_weights",

@@ -184,6 +184,16 @@ def swiglu_forward(A: torch.Tensor, Wpacked: torch.Tensor, N: int, Y: torch.Tens
     return swiglu_forward_variant(A, Wpacked, N, SWIGLU_VARIANT_AUTO, Y=Y, stream=stream)
 
 
+def pack(W1: torch.Tensor, W2: torch.Tensor) -> torch.Tensor:
+    """Short name of swiglu_pack_weights: the packed gate/up weight Wp from W1, W2 [K, N]."""
+    return swiglu_pack_weights(W1, W2)
+
+
+def forward(A: torch.Tensor, Wp: torch.Tensor, N: int) -> torch.Tensor:
+    """Short name of swiglu_forward: Y [M, N] = SiLU(A W1) * (A W2) on the current stream."""
+    return swiglu_forward(A, Wp, N)
+
+
 def _dev_fp8(t: torch.Tensor, name: str) -> None:
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
@@ -330,8 +340,9 @@ def swiglu_forward_noalloc(A: torch.Tensor, Wpacked: torch.Tensor, N: int, Y: to
                            status_out=None, stream=None) -> torch.Tensor:
     """Allocation-free decode forward (M <= 256) into a caller-provided Y.
 
-    `status_out`: optional ctypes uint32 array of 4 (host) that receives the
-    kernel's status record after the stream synchronises.
+    `status_out`: optional host buffer of 4 x 32-bit words that receives the
+    kernel's status record once the stream synchronises: a ctypes uint32
+    array, or a CPU int32 tensor (page-locked keeps the copy asynchronous).
     """
     _dev_bf16(A, "A")
     _dev_bf16(Wpacked, "Wpacked")
@@ -339,7 +350,17 @@ def swiglu_forward_noalloc(A: torch.Tensor, Wpacked: torch.Tensor, N: int, Y: to
     M, K = A.shape
     if tuple(Y.shape) != (M, N):
         raise ValueError("Y must be [M, N]")
-    ptr = ctypes.addressof(status_out) if status_out is not None else None
+    if status_out is None:
+        ptr = None
+    elif isinstance(status_out, torch.Tensor):
+        if (status_out.is_cuda or status_out.dtype != torch.int32 or status_out.numel() < 4
+                or not status_out.is_contiguous()):
+            raise ValueError("status_out must be a contiguous host int32 tensor of 4 words")
+        ptr = status_out.data_ptr()
+    else:
+        if ctypes.sizeof(status_out) < 16:
+            raise ValueError("status_out must hold 4 x uint32")
+        ptr = ctypes.addressof(status_out)
     with _on_device(A.device):
         _check(lib.swiglu_forward_noalloc(A.data_ptr(), Wpacked.data_ptr(), Y.data_ptr(), M, K, N,
                                           ptr, _stream_handle(stream, A.device)),

@@ -772,6 +772,8 @@ swiglu_status_t swiglu_forward_noalloc(const void* A, const void* Wpacked, void*
   p.mt = pl.mt;
   p.stages = pl.stages;
   p.grid = pl.grid;
+  p.splits = pl.splits;    // 1: no SM count, so no K split over clusters
+  p.mgroups = pl.mgroups;  // 1: one CTA per column block holds all M tokens
   p.status = s->scratch;
   p.timeout_ns = g_timeout_ns.load();
   p.inject_stall = g_inject.load();

@@ -1,44 +1,104 @@
 """The allocation-free entry point, swiglu_forward_noalloc (needs a GB300).
 
-It serves callers that cannot call cudaMalloc (code running under CUDA-graph
-stream capture, serving runtimes that reserve all device memory for their own
-pools, hosts that forbid allocation after start-up): the decode kernel runs
-with its status record in a static device array instead of library-allocated
-memory. Called here through the C ABI directly, twice in a row on different
-activations, and compared with swiglu_forward's output on the same inputs
-within the tests' tolerance |y - y_ref| <= 1e-2 |y_ref| + 1e-3. This file is
-collected last so that a run stopping at its first failure has run the rest.
+Some callers cannot let a library call cudaMalloc: serving runtimes that
+reserve all device memory for their own pools up front, and hosts that forbid
+allocation once start-up is over. For them the decode kernel runs with its
+status record in a static device array instead of library-allocated memory.
+
+Called here through the C ABI directly, twice in a row on different
+activations, and compared with the float64 oracle and with swiglu_forward's
+output on the same inputs, within the tests' tolerance
+|y - y_ref| <= 1e-2 |y_ref| + 1e-3. The shapes include those where its
+device-independent launch shape (one CTA per column block holding all
+tokens) differs from swiglu_forward's: more than 32 tokens, up to the 256-row
+limit (all 512 tensor-memory columns), narrow N (swiglu_forward would split K
+over clusters) and more column blocks than SMs (a second wave). A stalled
+pipeline wait must come back as status 4 and the next call as all zeros.
+This file is collected last so that a run stopping at its first failure has
+run every other test first.
 """
 import ctypes
 
 import pytest
 import torch
 
-from swiglu_gated_mlp_gb300.workloads import make_inputs
+from oracle import compare
+from oracle.swiglu_ref import swiglu_f64
+from swiglu_gated_mlp_gb300.workloads import bf16_bits, make_inputs
 
 pytestmark = pytest.mark.gpu
 
+CASES = [
+    (1, 512, 20480),    # 160 column blocks: more CTAs than SMs
+    (17, 256, 1408),    # narrow N: swiglu_forward splits K over clusters here
+    (48, 512, 18944),   # 148 column blocks, 48 tokens in one CTA per block
+    (100, 520, 1408),   # ragged K slice, narrow N
+    (128, 256, 18944),
+    (256, 384, 20480),  # the 256-row limit: 2 x 256 accumulator columns
+]
 
-def test_noalloc_matches_forward_on_two_calls_in_a_row(native_lib):
+
+def _status_buffer():
+    """Page-locked host buffer for the 4-word status record, filled with junk."""
+    return torch.full((4,), 7, dtype=torch.int32, pin_memory=True)
+
+
+def _noalloc(lib, a, wp, y, M, K, N, status, stream):
+    return lib.swiglu_forward_noalloc(a.data_ptr(), wp.data_ptr(), y.data_ptr(), M, K, N,
+                                      status.data_ptr(), stream)
+
+
+@pytest.mark.parametrize("M,K,N", CASES)
+def test_noalloc_matches_oracle_and_forward_on_two_calls_in_a_row(native_lib, M, K, N):
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
     lib = native_lib.lib
-    M, K, N = 16, 1024, 1408
-    _, w1, w2 = make_inputs(1, K, N, seed=40)
+    _, w1, w2 = make_inputs(1, K, N, seed=40 + M)
     wp = native_lib.swiglu_pack_weights(w1.cuda(), w2.cuda())
     stream = torch.cuda.current_stream().cuda_stream
     for call, seed in enumerate((41, 42)):
-        a = make_inputs(M, K, 8, seed=seed)[0].cuda()
-        y_ref = native_lib.swiglu_forward(a, wp, N)
+        a = make_inputs(M, K, 8, seed=seed + M)[0]
+        ad = a.cuda()
+        y_fwd = native_lib.swiglu_forward(ad, wp, N)
         y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
-        status = (ctypes.c_uint32 * 4)(7, 7, 7, 7)
-        rc = lib.swiglu_forward_noalloc(a.data_ptr(), wp.data_ptr(), y.data_ptr(), M, K, N,
-                                        ctypes.addressof(status), stream)
+        status = _status_buffer()
+        rc = _noalloc(lib, ad, wp, y, M, K, N, status, stream)
         assert rc == 0, native_lib.swiglu_status_string(rc)
         torch.cuda.synchronize()
-        assert list(status) == [0, 0, 0, 0], f"call {call}: status {list(status)}"
-        yf, rf = y.float(), y_ref.float()
-        assert torch.isfinite(yf).all()
+        assert status.tolist() == [0, 0, 0, 0], f"call {call}: status {status.tolist()}"
+        ref = swiglu_f64(bf16_bits(a), bf16_bits(w1), bf16_bits(w2))
+        rep = compare.report(bf16_bits(y.cpu()), ref)
+        assert rep["nonfinite"] == 0 and rep["tolerance_pass"], f"call {call}: {rep}"
+        yf, rf = y.float(), y_fwd.float()
         assert bool(((yf - rf).abs() <= 1e-2 * rf.abs() + 1e-3).all()), f"call {call}"
+
+
+def test_noalloc_reports_a_stalled_wait_then_recovers(native_lib):
+    # The testing hook leaves one pipeline stage unfilled, so a wait inside the
+    # kernel runs out after 200 ms; the kernel records status 4 in the shared
+    # array and stops cleanly. The next call starts from a cleared record.
+    lib = native_lib.lib
+    M, K, N = 16, 512, 1408
+    a, w1, w2 = make_inputs(M, K, N, seed=44)
+    wp = native_lib.swiglu_pack_weights(w1.cuda(), w2.cuda())
+    ad = a.cuda()
+    stream = torch.cuda.current_stream().cuda_stream
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    status = _status_buffer()
+    native_lib.swiglu_testing_inject_stall(True, 200)
+    try:
+        rc = _noalloc(lib, ad, wp, y, M, K, N, status, stream)
+        torch.cuda.synchronize()
+    finally:
+        native_lib.swiglu_testing_inject_stall(False, 1000)
+    assert rc == 0
+    assert status[0].item() == native_lib.SWIGLU_ERR_TIMEOUT, status.tolist()
+    assert status[3].item() >= 1, status.tolist()          # failures seen
+    status = _status_buffer()
+    assert _noalloc(lib, ad, wp, y, M, K, N, status, stream) == 0
+    torch.cuda.synchronize()
+    assert status.tolist() == [0, 0, 0, 0]
+    ref = swiglu_f64(bf16_bits(a), bf16_bits(w1), bf16_bits(w2))
+    assert compare.report(bf16_bits(y.cpu()), ref)["tolerance_pass"]
 
 
 def test_noalloc_rejects_sizes_beyond_its_limit(native_lib):
@@ -46,3 +106,8 @@ def test_noalloc_rejects_sizes_beyond_its_limit(native_lib):
     # M above the decode kernel's 256 rows: refused before any device work
     assert lib.swiglu_forward_noalloc(0x10000, 0x100000, 0x1000000, 300, 64, 64, None,
                                       None) == native_lib.SWIGLU_ERR_UNSUPPORTED
+    # M = 0: nothing to do, and the status record reads all zeros
+    st = (ctypes.c_uint32 * 4)(7, 7, 7, 7)
+    assert lib.swiglu_forward_noalloc(0x10000, 0x100000, 0x1000000, 0, 64, 64,
+                                      ctypes.addressof(st), None) == 0
+    assert list(st) == [0, 0, 0, 0]
