@@ -21,6 +21,10 @@ Efficient LLM Inference", gist.science technical summary):
 * ``pack_layout``: the packed gate/up weight layout, stated plainly; the pages
   concatenate W1 and W2 into one fused K x 2N matrix (section "Methodology /
   Kernel-2"); this library's layout is a block interleave of the same columns.
+* ``mxfp8``: the block-scaled FP8 reading (E4M3 values, one power-of-two
+  UE8M0 scale per 32 consecutive K values of A's rows and of W's columns) and
+  the byte layouts of its scale factors; the pages name FP8 only as a reason
+  the SwiGLU steps weigh more (section "Problem Statement").
 * ``compare``: the pass rule |y - ref| <= 1e-2 |ref| + 1e-3 and the mismatch
   rates (section "Key Contributions", numerical superiority: share of outputs
   with more than 1% relative error against a higher-precision reference).

@@ -125,3 +125,48 @@ def fp8_bits(t: torch.Tensor) -> np.ndarray:
     """The raw E4M3 bit patterns of a CPU float8 tensor as a numpy uint8 array."""
     assert t.dtype == torch.float8_e4m3fn
     return t.detach().cpu().contiguous().view(torch.uint8).numpy()
+
+
+MX_GROUP = 32  # K values that share one scale in the block-scaled FP8 inputs
+
+
+def _mx_quantise(x: torch.Tensor, dim: int):
+    """E4M3 values and UE8M0 scale exponents of x, one scale per 32 values along `dim`.
+
+    For each group, e = floor(log2(max|x|)) - 8 (E4M3's largest exponent is 8,
+    its largest value 448 = 1.75 * 2^8), clamped to [-127, 127]; the values are
+    x / 2^e rounded to nearest even in E4M3 after saturation to +-448, and the
+    stored scale byte is e + 127. All-zero groups get e = -127 (byte 0).
+    """
+    xt = x.movedim(dim, -1)
+    k = xt.shape[-1]
+    groups = -(-k // MX_GROUP)
+    pad = groups * MX_GROUP - k
+    xp = torch.nn.functional.pad(xt, (0, pad)) if pad else xt
+    xg = xp.reshape(*xp.shape[:-1], groups, MX_GROUP)
+    amax = xg.abs().amax(dim=-1)
+    e = torch.where(amax > 0, torch.floor(torch.log2(amax)) - 8, torch.full_like(amax, -127.0))
+    e = e.clamp(-127, 127)
+    q = (xg / torch.exp2(e).unsqueeze(-1)).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+    q = q.reshape(*xp.shape)[..., :k].movedim(-1, dim).contiguous()
+    s = (e + 127).to(torch.uint8).movedim(-1, dim).contiguous()
+    return q, s
+
+
+def make_inputs_mxfp8(M: int, K: int, N: int, seed: int):
+    """Block-scaled FP8 inputs for the MX path, from the same draws as ``make_inputs``.
+
+    The float32 draws (before any rounding) are quantised in groups of 32
+    consecutive K values: A's groups run along its rows, W1's and W2's down
+    their columns. Returns CPU tensors (A8 [M,K], SA [M,K/32], W1_8 [K,N],
+    S1 [K/32,N], W2_8 [K,N], S2 [K/32,N]); values float8_e4m3fn, scales uint8.
+    """
+    g = torch.Generator().manual_seed(int(seed))
+    a = torch.randn(M, K, generator=g, dtype=torch.float32)
+    scale = 1.0 / math.sqrt(K)
+    w1 = torch.randn(K, N, generator=g, dtype=torch.float32) * scale
+    w2 = torch.randn(K, N, generator=g, dtype=torch.float32) * scale
+    a8, sa = _mx_quantise(a, 1)
+    w18, s1 = _mx_quantise(w1, 0)
+    w28, s2 = _mx_quantise(w2, 0)
+    return a8, sa, w18, s1, w28, s2

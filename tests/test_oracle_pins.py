@@ -478,3 +478,126 @@ def test_down_pack_layout():
             b, t = divmod(k, 64)
             assert p[j, b, i, t] == w3[k, h]
     assert not p[1, :, 44:].any() and not p[:, 1, :, 36:].any()
+
+
+# ------------------------------------------------- block-scaled FP8 (MX) ----
+
+def test_ue8m0_decode_known_patterns():
+    from oracle.mxfp8 import ue8m0_to_f64
+    v = ue8m0_to_f64(np.array([0, 1, 126, 127, 128, 134, 254, 255], dtype=np.uint8))
+    assert v.tolist()[:7] == [2.0 ** -127, 2.0 ** -126, 0.5, 1.0, 2.0, 128.0, 2.0 ** 127]
+    assert np.isnan(v[7])
+
+
+def test_mx_reference_with_unit_scales_is_the_per_tensor_reference():
+    from oracle.fp8 import swiglu_f64_fp8
+    from oracle.mxfp8 import swiglu_f64_mxfp8
+    rng = np.random.default_rng(11)
+    a8 = rng.integers(0, 256, size=(4, 96), dtype=np.uint8)
+    w18 = rng.integers(0, 256, size=(96, 40), dtype=np.uint8)
+    w28 = rng.integers(0, 256, size=(96, 40), dtype=np.uint8)
+    for arr in (a8, w18, w28):
+        arr[(arr & 0x7F) == 0x7F] = 0x30                    # no NaN patterns
+    ones_a = np.full((4, 3), 127, dtype=np.uint8)
+    ones_w = np.full((3, 40), 127, dtype=np.uint8)
+    got = swiglu_f64_mxfp8(a8, ones_a, w18, ones_w, w28, ones_w)
+    assert np.array_equal(got, swiglu_f64_fp8(a8, w18, w28, 1.0, 1.0, 1.0))
+
+
+def _mx_brute(a8, sa, w18, s1, w28, s2):
+    """Pure-Python triple loop: every product scaled by its own two group exponents."""
+    import math as _m
+    from oracle.fp8 import e4m3_bits_to_f64
+    from oracle.brute import silu_scalar
+    av, w1v, w2v = (e4m3_bits_to_f64(x) for x in (a8, w18, w28))
+    M, K = a8.shape
+    N = w18.shape[1]
+    y = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            g = _m.fsum(_m.ldexp(float(av[m, k]) * float(w1v[k, n]),
+                                int(sa[m, k // 32]) + int(s1[k // 32, n]) - 254) for k in range(K))
+            u = _m.fsum(_m.ldexp(float(av[m, k]) * float(w2v[k, n]),
+                                int(sa[m, k // 32]) + int(s2[k // 32, n]) - 254) for k in range(K))
+            y[m, n] = silu_scalar(g) * u
+    return y
+
+
+@pytest.mark.parametrize("M,K,N", [(3, 64, 5), (2, 96, 7), (1, 32, 3)])
+def test_mx_reference_matches_brute_force(M, K, N):
+    from oracle.mxfp8 import swiglu_f64_mxfp8
+    rng = np.random.default_rng(M * 100 + K + N)
+    a8 = rng.integers(0, 0x78, size=(M, K), dtype=np.uint8) | (rng.integers(0, 2, size=(M, K)) << 7).astype(np.uint8)
+    w18 = rng.integers(0, 0x78, size=(K, N), dtype=np.uint8)
+    w28 = rng.integers(0x80, 0xF8, size=(K, N), dtype=np.uint8)
+    # scales that differ per group, per row of A and per column of W, so a
+    # scale applied along the wrong axis or to the wrong group is seen
+    sa = rng.integers(118, 136, size=(M, K // 32), dtype=np.uint8)
+    s1 = rng.integers(118, 136, size=(K // 32, N), dtype=np.uint8)
+    s2 = rng.integers(118, 136, size=(K // 32, N), dtype=np.uint8)
+    got = swiglu_f64_mxfp8(a8, sa, w18, s1, w28, s2)
+    want = _mx_brute(a8, sa, w18, s1, w28, s2)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-300)
+    # transposed scale arrays give a different result (the axis matters)
+    if K // 32 > 1:
+        wrong = swiglu_f64_mxfp8(a8, sa, w18, s1[::-1], w28, s2)
+        assert not np.allclose(wrong, want, rtol=1e-6)
+
+
+def test_mx_scale_is_an_exact_power_of_two_per_group():
+    # raising one group's exponent by 3 equals multiplying that group's values by 8
+    from oracle.mxfp8 import mx_values_rows, mx_values_cols
+    q = np.array([[0x38, 0x40, 0xB8] * 22], dtype=np.uint8)[:, :64]   # 1, 2, -1, ...
+    s = np.array([[127, 127]], dtype=np.uint8)
+    base = mx_values_rows(q, s)
+    s2 = s.copy()
+    s2[0, 1] += 3
+    got = mx_values_rows(q, s2)
+    assert np.array_equal(got[:, :32], base[:, :32])
+    assert np.array_equal(got[:, 32:], 8.0 * base[:, 32:])
+    # columns: the same along K for a [K, N] array
+    assert np.array_equal(mx_values_cols(q.T, s2.T), got.T)
+
+
+def test_scale_tile_layout_is_a_bijection_with_the_stated_offsets():
+    from oracle.mxfp8 import scale_tile_offset
+    r, g = np.meshgrid(np.arange(128), np.arange(4), indexing="ij")
+    off = scale_tile_offset(r, g)
+    assert sorted(off.ravel().tolist()) == list(range(512))
+    assert scale_tile_offset(0, 0) == 0 and scale_tile_offset(0, 3) == 3
+    assert scale_tile_offset(32, 0) == 4 and scale_tile_offset(1, 0) == 16
+    assert scale_tile_offset(127, 3) == 31 * 16 + 3 * 4 + 3
+
+
+def test_act_scale_tiles_element_by_element():
+    from oracle.mxfp8 import tile_act_scales, scale_tile_offset
+    rng = np.random.default_rng(12)
+    M, K = 130, 160                       # 2 row blocks, 2 K slices (the second ragged)
+    sa = rng.integers(0, 255, size=(M, K // 32), dtype=np.uint8)
+    t = tile_act_scales(sa, M, K)
+    assert t.size == 2 * 2 * 512
+    for m in range(256):
+        for grp in range(8):
+            blk = (m // 128) * 2 + grp // 4
+            got = t[blk * 512 + scale_tile_offset(m % 128, grp % 4)]
+            want = sa[m, grp] if (m < M and grp < K // 32) else 127
+            assert got == want
+
+
+def test_weight_scale_pack_element_by_element():
+    from oracle.mxfp8 import pack_weight_scales, scale_tile_offset
+    rng = np.random.default_rng(13)
+    K, N = 192, 136                       # 2 K slices (ragged), 2 column blocks (ragged)
+    s1 = rng.integers(0, 255, size=(K // 32, N), dtype=np.uint8)
+    s2 = rng.integers(0, 255, size=(K // 32, N), dtype=np.uint8)
+    p = pack_weight_scales(s1, s2, K, N)
+    assert p.size == 2 * 2 * 1024
+    for j in range(2):
+        for b in range(2):
+            tile = p[(j * 2 + b) * 1024:(j * 2 + b + 1) * 1024]
+            for half, src in ((0, s1), (1, s2)):
+                for i in range(128):
+                    for grp in range(4):
+                        n, kg = 128 * j + i, 4 * b + grp
+                        want = src[kg, n] if (n < N and kg < K // 32) else 127
+                        assert tile[half * 512 + scale_tile_offset(i, grp)] == want
