@@ -55,8 +55,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from swiglu_gated_mlp_gb300.workloads import (WORKLOADS, Workload, bf16_bits,  # noqa: E402
-                                              make_inputs, make_inputs_fp8, make_workload_inputs,
-                                              sample_rows, sweep_32b)
+                                              make_inputs, make_inputs_fp8, make_inputs_mxfp8,
+                                              make_workload_inputs, sample_rows, sweep_32b)
 
 METRIC = "fused SwiGLU-GEMM TFLOP/s (4·M·K·N) and % of GB300 dense BF16 peak"
 METRIC_DOWN = "MLP down-projection TFLOP/s (2·M·N·H), Out = Y·W3 + R"
@@ -254,14 +254,18 @@ class Prepared:
 def prepare(args, sg, w: Workload, dev) -> Prepared:
     """Inputs, packed weights and rotating copies for workload `w` on `dev`."""
     M, K, N = w.M, w.K, w.N
-    fp8 = args.dtype == "fp8"
+    mx = args.dtype == "mxfp8"
+    fp8 = args.dtype == "fp8" or mx
     down = args.op == "down"
     if down and fp8:
         raise SystemExit("--op down runs in bf16 only")
     elem = 1 if fp8 else 2
     flops = w.flops
     alg_bytes = elem * M * K + 2 * elem * K * N + 2 * M * N  # A, W1 and W2 once, Y (bf16)
+    if mx:  # one scale byte per 32 values of A, W1 and W2
+        alg_bytes += (M * K + 2 * K * N) // 32
     host = {}
+    SAs = None
     if down:
         # Out [M, H] = Y [M, N] x W3 [N, H] + R at this workload's MLP shape (H = K)
         H = K
@@ -271,6 +275,12 @@ def prepare(args, sg, w: Workload, dev) -> Prepared:
         r_cpu = make_inputs(M, H, 8, w.seed + 1)[0]
         wp0 = sg.swiglu_pack_down_weights(w3_cpu.to(dev))
         a_cpu = y_cpu
+    elif mx:
+        a_cpu, sa_cpu, w1_cpu, s1_cpu, w2_cpu, s2_cpu = make_inputs_mxfp8(M, K, N, w.seed)
+        wp0 = sg.swiglu_pack_weights_mxfp8(w1_cpu.to(dev), s1_cpu.to(dev), w2_cpu.to(dev),
+                                           s2_cpu.to(dev))
+        sat0 = sg.swiglu_pack_act_scales_mxfp8(sa_cpu.to(dev))
+        host["sat"] = sat0.cpu()
     elif fp8:
         a_cpu, w1_cpu, w2_cpu, scales = make_inputs_fp8(M, K, N, w.seed)
         wp0 = sg.swiglu_pack_weights_fp8(w1_cpu.to(dev), w2_cpu.to(dev))
@@ -297,36 +307,41 @@ def prepare(args, sg, w: Workload, dev) -> Prepared:
     out_cols = K if down else N
     Ys = [torch.empty(M, out_cols, dtype=torch.bfloat16, device=dev) for _ in range(copies)]
     Rs = None
+    if mx:
+        SAs = [sat0] + [sat0.clone() for _ in range(copies - 1)]
     if down:
         r0 = r_cpu.to(dev)
         Rs = [r0] + [r0.clone() for _ in range(copies - 1)]
     variant = VARIANTS[args.variant]
     plan = (sg.swiglu_down_plan_string(M, N, K) if down else
+            sg.swiglu_plan_string_mxfp8(M, K, N) if mx else
             sg.swiglu_plan_string_fp8(M, K, N) if fp8 else
             sg.swiglu_plan_string(M, K, N, variant))
-    base = plan.split(" ", 1)[1] if plan.startswith(("down ", "fp8 ")) else plan
+    base = plan.split(" ", 1)[1] if plan.startswith(("down ", "fp8 ", "mxfp8 ")) else plan
     kernel = ("fused_small_m_kernel" if base.startswith("small_m") else
               "fused_large_m_pair_kernel" if base.startswith("large_m_pair") else
               "fused_sequential_kernel" if base.startswith("sequential") else
               "fused_large_m_kernel")
-    if down or fp8:  # the template instance: <fp8> is E4M3 inputs, <down> the down-projection
-        kernel += "<down>" if down else "<fp8>"
+    if down or fp8:  # the template instance: <fp8> E4M3, <mxfp8> block-scaled, <down>
+        kernel += "<down>" if down else "<mxfp8>" if mx else "<fp8>"
 
     def fwd(j, s=None):
         """One forward on rotation slot j (on stream s, default the current stream)."""
         if down:
             sg.swiglu_down_forward(As[j], wps[j], K, R=Rs[j], Out=Ys[j], stream=s)
+        elif mx:
+            sg.swiglu_forward_mxfp8(As[j], SAs[j], wps[j], N, Y=Ys[j], stream=s)
         elif fp8:
             sg.swiglu_forward_fp8(As[j], wps[j], N, *scales, Y=Ys[j], stream=s)
         else:
             sg.swiglu_forward_variant(As[j], wps[j], N, variant, Y=Ys[j], stream=s)
 
-    if fp8:
+    if fp8 and not mx:
         host["scales"] = scales
     return Prepared(w=w, fp8=fp8, down=down, flops=flops, alg_bytes=alg_bytes, copies=copies,
                     plan=plan, kernel=kernel, fwd=fwd, out_cols=out_cols, w_bytes=w_bytes,
                     a_cpu=a_cpu, host=host,
-                    dev_state={"wps": wps, "As": As, "Ys": Ys, "Rs": Rs})
+                    dev_state={"wps": wps, "As": As, "Ys": Ys, "Rs": Rs, "SAs": SAs})
 
 
 def time_steps(args, sg, pr: Prepared, steps: int, world: int, dev, stream):
@@ -460,6 +475,10 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     e2e_streams = [stream, torch.cuda.Stream(device=dev)]
     a_dev = [torch.empty(*a_cpu.shape, dtype=a_cpu.dtype, device=dev) for _ in e2e_streams]
     y_dev = [torch.empty(M, out_cols, dtype=torch.bfloat16, device=dev) for _ in e2e_streams]
+    mx = "sat" in pr.host
+    if mx:  # A's block scales travel with A every step
+        sa_host = [pr.host["sat"].pin_memory() for _ in a_host]
+        sa_dev = [torch.empty_like(pr.host["sat"], device=dev) for _ in e2e_streams]
     e2e_steps = steps
 
     def e2e_step(i):
@@ -471,6 +490,13 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
                 a_dev[b].copy_(a_host[j], non_blocking=True)
                 sg.swiglu_down_forward(a_dev[b], wps[i % copies], K, R=Rs[i % copies],
                                        Out=y_dev[b], stream=st)
+                y_host[j].copy_(y_dev[b], non_blocking=True)
+        elif mx:  # host copies through torch around the block-scaled call
+            with torch.cuda.stream(st):
+                a_dev[b].copy_(a_host[j], non_blocking=True)
+                sa_dev[b].copy_(sa_host[j], non_blocking=True)
+                sg.swiglu_forward_mxfp8(a_dev[b], sa_dev[b], wps[i % copies], N, Y=y_dev[b],
+                                        stream=st)
                 y_host[j].copy_(y_dev[b], non_blocking=True)
         elif fp8:  # host copies through torch around the FP8 call
             with torch.cuda.stream(st):
@@ -494,10 +520,12 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     barrier(world)
     sg.swiglu_check_device_status(stream=stream)
     e2e = {"value": round(aggregate(pr.flops, e2e_steps, e2e_s, world), 3), "unit": "TFLOP/s",
-           "h2d_bytes_per_step": a_cpu.numel() * a_cpu.element_size(),
+           "h2d_bytes_per_step": a_cpu.numel() * a_cpu.element_size() + (
+               pr.host["sat"].numel() if mx else 0),
            "d2h_bytes_per_step": 2 * M * out_cols,
            "steps": e2e_steps, "streams": len(e2e_streams),
            "api": ("pinned-host copies + swiglu_down_forward" if down else
+                   "pinned-host copies (A and its block scales) + swiglu_forward_mxfp8" if mx else
                    "pinned-host copies + swiglu_forward_fp8" if fp8 else
                    "swiglu_forward_from_host")}
     del a_dev, y_dev, a_host, y_host, wps, Rs, e2e_step
@@ -508,7 +536,8 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
         "n_gpus": world,
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(elapsed_max / steps * 1e3, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp8-e4m3 (fp32 accumulate, bf16 out)" if fp8 else "bf16",
+        "dtype": ("mxfp8-e4m3 (UE8M0 scale per 32 K, fp32 accumulate, bf16 out)" if args.dtype == "mxfp8"
+                  else "fp8-e4m3 (fp32 accumulate, bf16 out)" if fp8 else "bf16"),
         "data": "synthetic",
         "config": {"workload": w.name, "M": M, "K": K, "N": N, "seed": w.seed,
                    "variant": args.variant, "inputs": args.dtype, "op": args.op,
@@ -856,8 +885,9 @@ def main(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--op", choices=["swiglu", "down"], default="swiglu",
                    help="swiglu: the fused gate/up projection (default); down: Out = Y W3 + R")
-    p.add_argument("--dtype", choices=["bf16", "fp8"], default="bf16",
-                   help="input type: bf16 (the metric's), or E4M3 with per-tensor scales")
+    p.add_argument("--dtype", choices=["bf16", "fp8", "mxfp8"], default="bf16",
+                   help="input type: bf16 (the metric's), E4M3 with per-tensor scales, or "
+                        "block-scaled E4M3 (one UE8M0 scale per 32 K values)")
     p.add_argument("--variant", choices=sorted(VARIANTS), default="auto",
                    help="kernel to time (default: the automatic choice)")
     p.add_argument("--eager", action="store_true",

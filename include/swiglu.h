@@ -220,6 +220,60 @@ SWIGLU_API swiglu_status_t swiglu_plan_string_fp8(int64_t M, int64_t K, int64_t 
                                                   size_t buflen);
 
 /*
+ * Block-scaled FP8 form of the op (MX: E4M3 values, one power-of-two scale per
+ * 32 consecutive K values). As for the per-tensor form, the pages name FP8
+ * only as the reason the SwiGLU steps weigh more once the GEMMs run faster
+ * ("Tile-Level Activation Overlap for Efficient LLM Inference", gist.science,
+ * section "Problem Statement"); they give no scaling scheme. Here:
+ *   A[m][k]  = A8[m][k]  * 2^(SA[m][k/32] - 127)
+ *   W1[k][n] = W1_8[k][n] * 2^(S1[k/32][n] - 127)      (W2 likewise with S2)
+ *   Y = SiLU(A x W1) (.) (A x W2)   (bf16 output, fp32 accumulation)
+ * Scales are UE8M0 bytes (value 2^(e - 127); 255 is NaN and must not occur);
+ * A's scales run along its rows, W's down its columns. The tensor cores apply
+ * both scales inside each MMA (tcgen05 kind::mxf8f6f4); no per-tensor factor.
+ * K must be a multiple of 32 (else UNSUPPORTED); N a multiple of 8.
+ *
+ * Scale blocks: one 512-byte block holds the scales of 128 rows x 4 groups
+ * (128 K values); row r, group g at byte (r % 32) * 16 + (r / 32) * 4 + g.
+ *
+ * swiglu_packed_weight_bytes_mxfp8(K, N): bytes of the packed weight: the
+ *   E4M3 values exactly as swiglu_pack_weights_fp8 lays them out (2 * Np * Kp
+ *   bytes, Kp = K rounded up to 128), followed by 1024 bytes per packed tile
+ *   (column block j, K slice b, same tile order): W1's scale block for columns
+ *   128j .. 128j+127 and groups 4b .. 4b+3, then W2's; 127 where no value is.
+ * swiglu_pack_weights_mxfp8: W1_8, W2_8 [K, N] E4M3 and S1, S2 [K/32, N]
+ *   UE8M0, row-major device arrays, into Wpacked (device, 16-byte aligned, of
+ *   swiglu_packed_weight_bytes_mxfp8 bytes, overlapping none of them).
+ * swiglu_act_scale_bytes_mxfp8(M, K): bytes of A's scales in blocks:
+ *   ceil(M/128) x ceil(K/128) blocks of 512 bytes, row-block major.
+ * swiglu_pack_act_scales_mxfp8: SA [M, K/32] UE8M0 row-major (device) into
+ *   that block layout (SAtiled, device, 16-byte aligned); 127 where no row or
+ *   group is. A producer of quantised activations may write the block layout
+ *   directly instead.
+ * swiglu_forward_mxfp8: A8 [M, K] E4M3 (device), SAtiled (from the call
+ *   above), Wpacked (from swiglu_pack_weights_mxfp8 with the same K, N), Y
+ *   [M, N] bf16 (device, written in full, overlapping no input). All 16-byte
+ *   aligned. M = 0 is a no-op. Few tokens (the FP8 decode rule, at most 128)
+ *   run the decode kernel, others the CTA-pair kernel.
+ * swiglu_plan_string_mxfp8: the kernel and launch shape swiglu_forward_mxfp8
+ *   chooses for (M, K, N) on the current device, as text ("mxfp8 ...").
+ * Errors as the bf16 calls.
+ */
+SWIGLU_API size_t swiglu_packed_weight_bytes_mxfp8(int64_t K, int64_t N);
+SWIGLU_API swiglu_status_t swiglu_pack_weights_mxfp8(const void* W1, const void* S1,
+                                                     const void* W2, const void* S2,
+                                                     void* Wpacked, int64_t K, int64_t N,
+                                                     swiglu_stream_t stream);
+SWIGLU_API size_t swiglu_act_scale_bytes_mxfp8(int64_t M, int64_t K);
+SWIGLU_API swiglu_status_t swiglu_pack_act_scales_mxfp8(const void* SA, void* SAtiled, int64_t M,
+                                                        int64_t K, swiglu_stream_t stream);
+SWIGLU_API swiglu_status_t swiglu_forward_mxfp8(const void* A, const void* SAtiled,
+                                                const void* Wpacked, void* Y, int64_t M,
+                                                int64_t K, int64_t N, swiglu_stream_t stream);
+SWIGLU_API swiglu_status_t swiglu_plan_string_mxfp8(int64_t M, int64_t K, int64_t N, char* buf,
+                                                   size_t buflen);
+
+/*
  * The gated MLP's down-projection, the step after Y in the models the pages
  * evaluate ("Tile-Level Activation Overlap for Efficient LLM Inference",
  * gist.science, section "Problem Statement": the SwiGLU gated MLP; the pages

@@ -13,6 +13,8 @@ is no CPU or PyTorch fallback.
 """
 _EXPORTS = {
     "pack", "forward",
+    "swiglu_packed_weight_bytes_mxfp8", "swiglu_pack_weights_mxfp8", "swiglu_act_scale_bytes_mxfp8",
+    "swiglu_pack_act_scales_mxfp8", "swiglu_forward_mxfp8", "swiglu_plan_string_mxfp8",
     "swiglu_pack_weights", "swiglu_forward", "swiglu_forward_variant", "swiglu_forward_from_host",
     "swiglu_forward_noalloc", "swiglu_pack_weights_fp8", "swiglu_forward_fp8",
     "swiglu_packed_weight_bytes_fp8", "swiglu_down_packed_bytes", "swiglu_pack_down_weights",

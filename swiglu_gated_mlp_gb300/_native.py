@@ -69,6 +69,18 @@ lib.swiglu_down_plan_string.argtypes = [_i64, _i64, _i64, ctypes.c_char_p, _sz]
 lib.swiglu_down_plan_string.restype = _int
 lib.swiglu_plan_string_fp8.argtypes = [_i64, _i64, _i64, ctypes.c_char_p, _sz]
 lib.swiglu_plan_string_fp8.restype = _int
+lib.swiglu_packed_weight_bytes_mxfp8.argtypes = [_i64, _i64]
+lib.swiglu_packed_weight_bytes_mxfp8.restype = _sz
+lib.swiglu_pack_weights_mxfp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _vp]
+lib.swiglu_pack_weights_mxfp8.restype = _int
+lib.swiglu_act_scale_bytes_mxfp8.argtypes = [_i64, _i64]
+lib.swiglu_act_scale_bytes_mxfp8.restype = _sz
+lib.swiglu_pack_act_scales_mxfp8.argtypes = [_vp, _vp, _i64, _i64, _vp]
+lib.swiglu_pack_act_scales_mxfp8.restype = _int
+lib.swiglu_forward_mxfp8.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]
+lib.swiglu_forward_mxfp8.restype = _int
+lib.swiglu_plan_string_mxfp8.argtypes = [_i64, _i64, _i64, ctypes.c_char_p, _sz]
+lib.swiglu_plan_string_mxfp8.restype = _int
 lib.swiglu_forward_noalloc.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp]
 lib.swiglu_forward_noalloc.restype = _int
 lib.swiglu_testing_inject_stall.argtypes = [_int, _u32]
@@ -248,6 +260,98 @@ def swiglu_forward_fp8(A: torch.Tensor, Wpacked: torch.Tensor, N: int, scale_a: 
                                       _stream_handle(stream, A.device)),
                "swiglu_forward_fp8")
     return Y
+
+
+def _dev_u8(t: torch.Tensor, name: str) -> None:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != torch.uint8:
+        raise ValueError(f"{name} must be uint8 (UE8M0 scale bytes), got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def swiglu_packed_weight_bytes_mxfp8(K: int, N: int) -> int:
+    return int(lib.swiglu_packed_weight_bytes_mxfp8(int(K), int(N)))
+
+
+def swiglu_act_scale_bytes_mxfp8(M: int, K: int) -> int:
+    return int(lib.swiglu_act_scale_bytes_mxfp8(int(M), int(K)))
+
+
+def swiglu_pack_weights_mxfp8(W1: torch.Tensor, S1: torch.Tensor, W2: torch.Tensor,
+                              S2: torch.Tensor, Wpacked: torch.Tensor | None = None,
+                              stream=None) -> torch.Tensor:
+    """Packed block-scaled weight (flat uint8) from E4M3 W1, W2 [K, N] and UE8M0 S1, S2 [K/32, N]."""
+    _dev_fp8(W1, "W1")
+    _dev_fp8(W2, "W2")
+    _dev_u8(S1, "S1")
+    _dev_u8(S2, "S2")
+    if W1.dim() != 2 or W1.shape != W2.shape:
+        raise ValueError("W1 and W2 must both be [K, N]")
+    K, N = W1.shape
+    if tuple(S1.shape) != (K // 32, N) or tuple(S2.shape) != (K // 32, N):
+        raise ValueError("S1 and S2 must be [K/32, N]")
+    if Wpacked is None:
+        Wpacked = torch.empty(swiglu_packed_weight_bytes_mxfp8(K, N), dtype=torch.uint8,
+                              device=W1.device)
+    if Wpacked.numel() * Wpacked.element_size() < swiglu_packed_weight_bytes_mxfp8(K, N):
+        raise ValueError("Wpacked is too small")
+    with _on_device(W1.device):
+        _check(lib.swiglu_pack_weights_mxfp8(W1.data_ptr(), S1.data_ptr(), W2.data_ptr(),
+                                             S2.data_ptr(), Wpacked.data_ptr(), K, N,
+                                             _stream_handle(stream, W1.device)),
+               "swiglu_pack_weights_mxfp8")
+    return Wpacked
+
+
+def swiglu_pack_act_scales_mxfp8(SA: torch.Tensor, SAtiled: torch.Tensor | None = None,
+                                 stream=None) -> torch.Tensor:
+    """A's UE8M0 scales [M, K/32] in the 512-byte block layout the forward reads."""
+    _dev_u8(SA, "SA")
+    if SA.dim() != 2:
+        raise ValueError("SA must be [M, K/32]")
+    M, K = SA.shape[0], 32 * SA.shape[1]
+    if SAtiled is None:
+        SAtiled = torch.empty(max(swiglu_act_scale_bytes_mxfp8(M, K), 16), dtype=torch.uint8,
+                              device=SA.device)
+    if SAtiled.numel() * SAtiled.element_size() < swiglu_act_scale_bytes_mxfp8(M, K):
+        raise ValueError("SAtiled is too small")
+    with _on_device(SA.device):
+        _check(lib.swiglu_pack_act_scales_mxfp8(SA.data_ptr(), SAtiled.data_ptr(), M, K,
+                                                _stream_handle(stream, SA.device)),
+               "swiglu_pack_act_scales_mxfp8")
+    return SAtiled
+
+
+def swiglu_forward_mxfp8(A: torch.Tensor, SAtiled: torch.Tensor, Wpacked: torch.Tensor, N: int,
+                         Y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Y [M, N] bf16 = SiLU(A x W1) * (A x W2) from block-scaled E4M3 A [M, K] and the packed weight."""
+    _dev_fp8(A, "A")
+    if A.dim() != 2:
+        raise ValueError("A must be [M, K]")
+    M, K = A.shape
+    if Wpacked.numel() * Wpacked.element_size() < swiglu_packed_weight_bytes_mxfp8(K, N):
+        raise ValueError("Wpacked does not hold a packed block-scaled weight for this K and N")
+    if SAtiled.numel() * SAtiled.element_size() < swiglu_act_scale_bytes_mxfp8(M, K):
+        raise ValueError("SAtiled does not hold A's scales for this M and K")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _dev_bf16(Y, "Y")
+    if tuple(Y.shape) != (M, N):
+        raise ValueError("Y must be [M, N]")
+    with _on_device(A.device):
+        _check(lib.swiglu_forward_mxfp8(A.data_ptr(), SAtiled.data_ptr(), Wpacked.data_ptr(),
+                                        Y.data_ptr(), M, K, N, _stream_handle(stream, A.device)),
+               "swiglu_forward_mxfp8")
+    return Y
+
+
+def swiglu_plan_string_mxfp8(M: int, K: int, N: int) -> str:
+    buf = ctypes.create_string_buffer(256)
+    _check(lib.swiglu_plan_string_mxfp8(int(M), int(K), int(N), buf, 256),
+           "swiglu_plan_string_mxfp8")
+    return buf.value.decode()
 
 
 def swiglu_down_packed_bytes(N: int, H: int) -> int:

@@ -20,7 +20,13 @@
 //    (tcgen05.ld -> SiLU * mul in fp32 registers -> bf16 -> swizzled shared
 //    staging -> TMA store) overlaps the MMAs of tile i+1;
 //  * every pipeline wait is bounded (see ptx.cuh); a stuck wait aborts the
-//    CTA cleanly and is reported through the status word.
+//    CTA cleanly and is reported through the status word;
+//  * on long K loops (at least 4 ring-fulls) an idle epilogue warp asks L2,
+//    before the grid-dependency wait, to fetch the first packed weight slices
+//    of the CTA's first tile (about 64 MB over the grid) and a share of its A
+//    rows, so the first DRAM reads start under the previous grid's tail. On
+//    short loops (the 0.5B shape: 14 slices, 8 stages) staging measured
+//    slower, so it is off there.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -99,6 +105,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
+  }
+  if (warp == 2 && lane == 0 && p.l2_prefetch > 0 && num_kb >= 4 * C::kStages &&
+      static_cast<int>(blockIdx.x) < num_tiles) {
+    // Inputs of the step, not products of the kernel before it in the stream;
+    // L2 is coherent, so loads after the wait still see any write that kernel
+    // made.
+    int mb, nb;
+    tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, p.group_m, mb, nb);
+    const int col0 = nb * BN;
+    const int wtile = (col0 / kPackBlockN) * num_kb;
+    const int wrow = col0 % kPackBlockN;
+    const uint64_t pol = policy_evict_first();
+    const int nw = min(p.l2_prefetch, num_kb);
+    for (int kb = 0; kb < nw; ++kb) {
+      tma_prefetch_l2_3d_hint(&p.tmap_w, 0, wrow, wtile + kb, pol);
+      tma_prefetch_l2_3d_hint(&p.tmap_w, 0, wrow + kPackBlockN, wtile + kb, pol);
+    }
+    // A's rows are shared by the CTAs of a row tile: each takes every 8th slice
+    for (int kb = static_cast<int>(blockIdx.x % 8u); kb < nw; kb += 8)
+      tma_prefetch_l2_2d(&p.tmap_a, kb * kBlockK, mb * kTileM);
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);

@@ -25,6 +25,15 @@
 // Out = Y x W3 + R: a tile is 256 consecutive output columns (rank r loads
 // packed rows [128 r, 128 r + 128) of W3's tile), and the epilogue stores
 // accumulator + residual for all 256 columns.
+//
+// With kMx (block-scaled E4M3: one power-of-two scale per 32 K values) each
+// CTA also loads, per stage, the scale block of its 128 A rows and both of the
+// packed tile's weight-scale blocks (gate, up: the MMA's 256 B columns); the
+// even CTA copies them into a per-stage slot of both CTAs' tensor memory
+// (tcgen05.cp.cta_group::2, each CTA from its own shared memory) and issues
+// kind::mxf8f6f4 MMAs. The scale slots take the second half of tensor memory,
+// so the accumulator is single-buffered: the next tile's MMAs wait for the
+// epilogue to have read the previous one.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -45,6 +54,11 @@ struct PairCfg {
   static constexpr size_t kSmem =
       1024 + size_t(kStages) * kStageBytes + size_t(kNumStg) * kStgBytes + kBarBytes;
   static_assert(kSmem <= 232448, "shared memory budget");
+  // block-scaled FP8: 1.5 KB of scales per stage (A block, gate and up weight blocks)
+  static constexpr size_t kSmemMx = kSmem + size_t(kStages) * kSfStageBytes;
+  static_assert(kSmemMx <= 232448, "shared memory budget (block-scaled)");
+  static constexpr int kSfCol = kAccCols;  // scale slots after the single accumulator
+  static_assert(kSfCol + kStages * kSfTmemCols <= kTmemCols, "tensor memory budget");
 };
 
 __device__ __forceinline__ void pair_tile_coords(int t, int tiles_m, int tiles_n, int group_m,
@@ -58,10 +72,12 @@ __device__ __forceinline__ void pair_tile_coords(int t, int tiles_m, int tiles_n
   nb = r / gm;
 }
 
-template <bool kFp8, bool kDown>
+template <bool kFp8, bool kDown, bool kMx>
 __global__ void __launch_bounds__(kThreads, 1)
     fused_large_m_pair_kernel(const __grid_constant__ LargeMParams p) {
   using C = PairCfg;
+  static_assert(!kMx || (kFp8 && !kDown), "block scales go with E4M3 gate/up inputs");
+  constexpr int kAccBufs = kMx ? 1 : 2;  // accumulator buffers in tensor memory
   // K values per stage: 64 bf16 or 128 E4M3, a 128-byte row either way
   constexpr int kBK = kFp8 ? kBlockK8 : kBlockK;
   extern __shared__ uint8_t smem_raw[];
@@ -70,7 +86,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sA = smem_addr(smem);
   const uint32_t sB = sA + C::kStages * C::kABytes;
   const uint32_t sStg = sB + C::kStages * C::kBBytes;
-  uint8_t* bar_ptr = smem + size_t(C::kStages) * C::kStageBytes + C::kNumStg * C::kStgBytes;
+  const uint32_t sSf = sStg + C::kNumStg * C::kStgBytes;  // scales (kMx): kStages x 1.5 KB
+  uint8_t* bar_ptr = smem + size_t(C::kStages) * C::kStageBytes + C::kNumStg * C::kStgBytes +
+                     (kMx ? size_t(C::kStages) * kSfStageBytes : 0);
   const uint32_t bar0 = smem_addr(bar_ptr);
   // barrier slots: full[S] | empty[S] | tmem_full[2] | tmem_empty[2] | drain
   const uint32_t full0 = bar0, empty0 = bar0 + 8u * C::kStages;
@@ -96,6 +114,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&p.tmap_a);
     prefetch_tmap(&p.tmap_w);
     prefetch_tmap(&p.tmap_y);
+    if constexpr (kMx) {
+      prefetch_tmap(&p.tmap_sw);
+      prefetch_tmap(&p.tmap_sa);
+    }
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(full0 + 8u * s, 1);   // rank 0's producer arrives (with both CTAs' bytes)
       mbar_init(empty0 + 8u * s, 1);  // rank 0's MMA commit, multicast to both CTAs
@@ -140,10 +162,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (skip_once) {
             skip_once = false;  // testing hook: both CTAs leave this stage unfilled
           } else {
-            if (leader) mbar_arrive_expect_tx(full0 + 8u * s, 2 * C::kStageBytes);
+            if (leader)
+              mbar_arrive_expect_tx(full0 + 8u * s, 2 * (C::kStageBytes + (kMx ? kSfStageBytes : 0)));
             const uint32_t fb = full0_lead + 8u * s;
             tma_load_2d_pair(sA + s * C::kABytes, &p.tmap_a, fb, kb * kBK, m0);
             tma_load_3d_pair(sB + s * C::kBBytes, &p.tmap_w, fb, 0, wrow, wtile + kb);
+            if constexpr (kMx) {
+              // this CTA's A rows: block (m0 / 128, kb), 2 rows of 256 bytes; both
+              // weight-scale blocks of the tile (gate, up), 4 rows
+              const uint32_t sf = sSf + s * kSfStageBytes;
+              tma_load_2d_pair(sf, &p.tmap_sa, fb, 0, 2 * ((m0 / kTileM) * num_kb + kb));
+              tma_load_2d_pair(sf + kSfBlockBytes, &p.tmap_sw, fb, 0, 4 * (wtile + kb));
+            }
             filled |= 1u << s;
             fill_ph = (fill_ph & ~(1u << s)) | (ph << s);
           }
@@ -166,6 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (leader && lane == 0) {
       constexpr uint32_t kIdesc = kFp8 ? idesc_e4m3_f32(2 * kTileM, 2 * C::kBN)
                                        : idesc_bf16_f32(2 * kTileM, 2 * C::kBN);
+      constexpr uint32_t kIdescMx = idesc_mx_e4m3(2 * kTileM, 2 * C::kBN, 0);
       int s = 0;
       uint32_t ph = 0;
       int buf = 0;
@@ -183,9 +214,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint64_t adesc = smem_desc_sw128(sA + s * C::kABytes);
           const uint64_t bdesc = smem_desc_sw128(sB + s * C::kBBytes);
+          // scale slot of this stage: A rows [0, 4), B columns 0..127 [4, 8), 128..255 [8, 12)
+          const uint32_t tsf = tmem_base + C::kSfCol + uint32_t(s) * kSfTmemCols;
+          if constexpr (kMx) {
+            const uint32_t sf = sSf + s * kSfStageBytes;
+            tmem_cp_sf_pair(tsf, smem_desc_sf(sf));
+            tmem_cp_sf_pair(tsf + 4, smem_desc_sf(sf + kSfBlockBytes));
+            tmem_cp_sf_pair(tsf + 8, smem_desc_sf(sf + 2 * kSfBlockBytes));
+          }
 #pragma unroll
           for (int k = 0; k < 4; ++k) {  // four 32-byte K steps per 128-byte row
-            if constexpr (kFp8)
+            if constexpr (kMx)  // K step k consumes scale group k of the slice (IDs at bits 4, 29)
+              mma_mx_pair(d, adesc + 2u * k, bdesc + 2u * k,
+                          kIdescMx | (uint32_t(k) << 4) | (uint32_t(k) << 29), tsf, tsf + 4,
+                          (kb | k) != 0 ? 1u : 0u);
+            else if constexpr (kFp8)
               mma_e4m3_pair(d, adesc + 2u * k, bdesc + 2u * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
             else
               mma_bf16_pair(d, adesc + 2u * k, bdesc + 2u * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
@@ -198,8 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         mma_commit_pair_multicast(tfull0 + 8u * buf, 0x3);  // both halves of the accumulator ready
-        buf ^= 1;
-        if (buf == 0) acc_ph ^= 1u;
+        if (++buf == kAccBufs) {
+          buf = 0;
+          acc_ph ^= 1u;
+        }
       }
       mma_commit_pair_multicast(drain_bar, 0x1);
       mbar_wait_drain(drain_bar, 0, wc);
@@ -319,8 +364,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           sbuf ^= 1;
         }
       }
-      buf ^= 1;
-      if (buf == 0) acc_ph ^= 1u;
+      if (++buf == kAccBufs) {
+        buf = 0;
+        acc_ph ^= 1u;
+      }
     }
     if (lane == 0) bulk_wait<0>();
     __syncwarp();
@@ -337,11 +384,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr,
-                               bool with_pdl) {
+                               bool with_pdl, bool mx = false) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = PairCfg::kSmem;
+  cfg.dynamicSmemBytes = mx ? PairCfg::kSmemMx : PairCfg::kSmem;
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -357,22 +404,26 @@ cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribut
 }  // namespace
 
 cudaError_t configure_large_m_pair(int* max_pairs) {
-  cudaError_t e = cudaFuncSetAttribute(fused_large_m_pair_kernel<false, false>,
+  cudaError_t e = cudaFuncSetAttribute(fused_large_m_pair_kernel<false, false, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(PairCfg::kSmem));
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(fused_large_m_pair_kernel<true, false>,
+    e = cudaFuncSetAttribute(fused_large_m_pair_kernel<true, false, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(PairCfg::kSmem));
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(fused_large_m_pair_kernel<false, true>,
+    e = cudaFuncSetAttribute(fused_large_m_pair_kernel<false, true, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(PairCfg::kSmem));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fused_large_m_pair_kernel<true, false, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(PairCfg::kSmemMx));
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pair_config(2, nullptr, attr, false);
   int clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&clusters, fused_large_m_pair_kernel<false, false>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&clusters, fused_large_m_pair_kernel<false, false, false>, &cfg);
   if (e != cudaSuccess) return e;
   *max_pairs = clusters;
   return cudaSuccess;
@@ -384,12 +435,14 @@ int large_m_pair_stages() { return PairCfg::kStages; }
 cudaError_t launch_large_m_pair(const LargeMParams& p, cudaStream_t stream) {
   if (p.grid < 2 || (p.grid % 2) != 0 || p.bn != PairCfg::kBN) return cudaErrorInvalidValue;
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = pair_config(p.grid, stream, attr, pdl_enabled());
+  cudaLaunchConfig_t cfg = pair_config(p.grid, stream, attr, pdl_enabled(), p.mx != 0);
   if (p.fp8 && p.down) return cudaErrorInvalidValue;  // no FP8 down-projection
+  if (p.mx && !p.fp8) return cudaErrorInvalidValue;   // block scales go with E4M3 values
   const cudaError_t e =
-      p.down ? cudaLaunchKernelEx(&cfg, fused_large_m_pair_kernel<false, true>, p)
-      : p.fp8 ? cudaLaunchKernelEx(&cfg, fused_large_m_pair_kernel<true, false>, p)
-              : cudaLaunchKernelEx(&cfg, fused_large_m_pair_kernel<false, false>, p);
+      p.down  ? cudaLaunchKernelEx(&cfg, fused_large_m_pair_kernel<false, true, false>, p)
+      : p.mx  ? cudaLaunchKernelEx(&cfg, fused_large_m_pair_kernel<true, false, true>, p)
+      : p.fp8 ? cudaLaunchKernelEx(&cfg, fused_large_m_pair_kernel<true, false, false>, p)
+              : cudaLaunchKernelEx(&cfg, fused_large_m_pair_kernel<false, false, false>, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

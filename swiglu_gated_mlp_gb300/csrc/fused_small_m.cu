@@ -26,6 +26,12 @@
 // (kDown): a packed tile then holds 256 consecutive output columns, the two
 // accumulators are columns [0, 128) and [128, 256) of the block, and the
 // epilogue adds the residual instead of applying SiLU(g) * u.
+//
+// With kMx (block-scaled E4M3, one power-of-two scale per 32 K values) each
+// stage also brings the tile's two 512-byte weight-scale blocks (gate, up)
+// and the activations' scale block for the same K slice; the MMA thread copies
+// them into a per-stage slot of tensor memory (tcgen05.cp) and issues
+// kind::mxf8f6f4 MMAs that apply both scales inside the tensor core.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -45,9 +51,10 @@ constexpr int kMaxStages = 8;
 constexpr size_t kSmemLimit = 232448;
 constexpr int kBarBytes = 256;
 
-template <bool kFp8, bool kDown>
+template <bool kFp8, bool kDown, bool kMx>
 __global__ void __launch_bounds__(kThreads, 1)
     fused_small_m_kernel(const __grid_constant__ SmallMParams p) {
+  static_assert(!kMx || (kFp8 && !kDown), "block scales go with E4M3 gate/up inputs");
   // K values per stage: 64 bf16 or 128 E4M3, a 128-byte row either way
   constexpr int kBK = kFp8 ? kBlockK8 : kBlockK;
   extern __shared__ uint8_t smem_raw[];
@@ -58,7 +65,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t x_bytes = static_cast<uint32_t>(mt) * 128;
   const uint32_t stage_bytes = kWStageBytes + x_bytes;  // multiple of 1024 (mt % 8 == 0)
   const uint32_t s0 = smem_addr(smem);
-  uint8_t* bar_ptr = smem + size_t(stages) * stage_bytes;
+  // block-scaled FP8: per stage 1.5 KB of scales (gate, up, activations) after the ring
+  const uint32_t sf0 = s0 + stages * stage_bytes;
+  uint8_t* bar_ptr = smem + size_t(stages) * stage_bytes + (kMx ? size_t(stages) * kSfStageBytes : 0);
   const uint32_t bar0 = smem_addr(bar_ptr);
   // barrier slots: full[8] | empty[8] | tmem_full | drain
   const uint32_t full0 = bar0, empty0 = bar0 + 8u * kMaxStages;
@@ -66,8 +75,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_ptr + 8 * (2 * kMaxStages + 2));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
+  // accumulators: gate [0, mt), up [mt, 2 mt); then kSfTmemCols scale columns per stage
+  const uint32_t sf_col = 2u * mt;
   uint32_t tmem_cols = 32;
-  while (tmem_cols < 2u * mt) tmem_cols <<= 1;
+  while (tmem_cols < sf_col + (kMx ? uint32_t(kSfTmemCols) * stages : 0u)) tmem_cols <<= 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -87,6 +98,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     prefetch_tmap(&p.tmap_x);
     prefetch_tmap(&p.tmap_w);
+    if constexpr (kMx) {
+      prefetch_tmap(&p.tmap_sw);
+      prefetch_tmap(&p.tmap_sa);
+    }
     // The packed weight is an input of the decode step, not a product of the
     // kernel before it in the stream; fetching this CTA's first tiles into L2
     // before the grid-dependency wait overlaps their DRAM latency with the
@@ -133,9 +148,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb = full0 + 8u * s;
           const uint32_t sw = s0 + s * stage_bytes;
           const int k0 = kb * kBK;
-          mbar_arrive_expect_tx(fb, stage_bytes);
+          mbar_arrive_expect_tx(fb, stage_bytes + (kMx ? kSfStageBytes : 0));
           tma_load_3d_hint(sw, &p.tmap_w, fb, 0, 0, wtile + kb, pol_w);  // one contiguous 32 KB tile
           tma_load_2d_hint(sw + kWStageBytes, &p.tmap_x, fb, k0, m0, pol_x);
+          if constexpr (kMx) {
+            // 4 rows of 256 bytes: the tile's gate and up scale blocks; 2 rows: the
+            // activations' block (128-row chunk m0 / 128, K slice kb)
+            const uint32_t sf = sf0 + s * kSfStageBytes;
+            tma_load_2d(sf, &p.tmap_sw, fb, 0, 4 * (wtile + kb));
+            tma_load_2d(sf + 2 * kSfBlockBytes, &p.tmap_sa, fb, 0, 2 * ((m0 / 128) * num_kb + kb));
+          }
           filled |= 1u << s;
           fill_ph = (fill_ph & ~(1u << s)) | (ph << s);
         }
@@ -168,10 +190,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t gdesc = smem_desc_sw128(sw);                         // gate rows 0..127
         const uint64_t udesc = smem_desc_sw128(sw + kWStageBytes / 2);      // up rows 128..255
         const uint64_t xdesc = smem_desc_sw128(sw + kWStageBytes);          // tokens
+        // scale slot of this stage: gate [0, 4), up [4, 8), tokens [8, 12)
+        const uint32_t tsf = tmem_base + sf_col + uint32_t(s) * kSfTmemCols;
+        if constexpr (kMx) {
+          const uint32_t sf = sf0 + s * kSfStageBytes;
+          tmem_cp_sf(tsf, smem_desc_sf(sf));
+          tmem_cp_sf(tsf + 4, smem_desc_sf(sf + kSfBlockBytes));
+          tmem_cp_sf(tsf + 8, smem_desc_sf(sf + 2 * kSfBlockBytes));
+        }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {  // four 32-byte K steps per 128-byte row
           const uint32_t acc = (kb != kb_begin || k != 0) ? 1u : 0u;
-          if constexpr (kFp8) {
+          if constexpr (kMx) {  // K step k consumes scale group k of the slice
+            const uint32_t id = idesc_mx_e4m3(128, mt, k);
+            mma_mx(d_gate, gdesc + 2u * k, xdesc + 2u * k, id, tsf, tsf + 8, acc);
+            mma_mx(d_up, udesc + 2u * k, xdesc + 2u * k, id, tsf + 4, tsf + 8, acc);
+          } else if constexpr (kFp8) {
             mma_e4m3(d_gate, gdesc + 2u * k, xdesc + 2u * k, idesc, acc);
             mma_e4m3(d_up, udesc + 2u * k, xdesc + 2u * k, idesc, acc);
           } else {
@@ -341,34 +375,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-int small_m_stages(int mt, int ctas_per_sm) {
+int small_m_stages(int mt, int ctas_per_sm, int extra) {
   // Shared memory per SM is 228 KB, of which 1 KB per resident CTA is reserved.
   const size_t per_cta = ctas_per_sm <= 1 ? kSmemLimit : (233472 - 2048) / 2;
-  const size_t stage = kWStageBytes + size_t(mt) * kBlockK * 2;
+  const size_t stage = kWStageBytes + size_t(mt) * kBlockK * 2 + size_t(extra);
   size_t s = (per_cta - 1024 - kBarBytes) / stage;
   if (s > kMaxStages) s = kMaxStages;
   return static_cast<int>(s);
 }
 
-size_t small_m_smem_bytes(int mt, int stages) {
-  return 1024 + size_t(stages) * (kWStageBytes + size_t(mt) * kBlockK * 2) + kBarBytes;
+size_t small_m_smem_bytes(int mt, int stages, int extra) {
+  return 1024 + size_t(stages) * (kWStageBytes + size_t(mt) * kBlockK * 2 + size_t(extra)) +
+         kBarBytes;
 }
 
-template <bool kFp8, bool kDown>
+template <bool kFp8, bool kDown, bool kMx>
 cudaError_t configure_small_m_t() {
-  cudaError_t e = cudaFuncSetAttribute(fused_small_m_kernel<kFp8, kDown>,
+  cudaError_t e = cudaFuncSetAttribute(fused_small_m_kernel<kFp8, kDown, kMx>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemLimit));
   if (e == cudaSuccess)  // all of the unified L1/shared array as shared memory (2 CTAs may share an SM)
-    e = cudaFuncSetAttribute(fused_small_m_kernel<kFp8, kDown>,
+    e = cudaFuncSetAttribute(fused_small_m_kernel<kFp8, kDown, kMx>,
                              cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   return e;
 }
 
 cudaError_t configure_small_m() {
-  cudaError_t e = configure_small_m_t<false, false>();
-  if (e == cudaSuccess) e = configure_small_m_t<true, false>();
-  if (e == cudaSuccess) e = configure_small_m_t<false, true>();
+  cudaError_t e = configure_small_m_t<false, false, false>();
+  if (e == cudaSuccess) e = configure_small_m_t<true, false, false>();
+  if (e == cudaSuccess) e = configure_small_m_t<false, true, false>();
+  if (e == cudaSuccess) e = configure_small_m_t<true, false, true>();
   return e;
 }
 
@@ -395,7 +431,7 @@ int small_m_max_clusters(int splits) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, fused_small_m_kernel<false, false>, &cfg) !=
+  if (cudaOccupancyMaxActiveClusters(&clusters, fused_small_m_kernel<false, false, false>, &cfg) !=
       cudaSuccess) {
     cudaGetLastError();
     return 0;
@@ -414,12 +450,18 @@ cudaError_t launch_small_m(const SmallMParams& p, cudaStream_t stream) {
        size_t(2) * p.mt * kPackBlockN * 4 > size_t(p.stages) * (kWStageBytes + size_t(p.mt) * kBlockK * 2) ||
        (p.grid % splits) != 0))
     return cudaErrorInvalidValue;
+  // block-scaled FP8: one 128-token group (the scale blocks cover 128 rows
+  // from m0 = 0) and 2 mt accumulator columns + the scale slots within 512
+  if (p.mx && (!p.fp8 || p.down || (p.mgroups > 1) || p.mt > 128 ||
+               2 * p.mt + kSfTmemCols * p.stages > 512))
+    return cudaErrorInvalidValue;
+  const int extra = p.mx ? kSfStageBytes : 0;
   SmallMParams q = p;
   q.l2_prefetch = small_m_l2_prefetch(p.grid, p.splits);
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(p.grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = small_m_smem_bytes(p.mt, p.stages);
+  cfg.dynamicSmemBytes = small_m_smem_bytes(p.mt, p.stages, extra);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -432,9 +474,10 @@ cudaError_t launch_small_m(const SmallMParams& p, cudaStream_t stream) {
   cfg.numAttrs = splits > 1 ? 2 : 1;
   if (p.fp8 && p.down) return cudaErrorInvalidValue;  // no FP8 down-projection
   const cudaError_t e =
-      p.down ? cudaLaunchKernelEx(&cfg, fused_small_m_kernel<false, true>, q)
-      : p.fp8 ? cudaLaunchKernelEx(&cfg, fused_small_m_kernel<true, false>, q)
-              : cudaLaunchKernelEx(&cfg, fused_small_m_kernel<false, false>, q);
+      p.down  ? cudaLaunchKernelEx(&cfg, fused_small_m_kernel<false, true, false>, q)
+      : p.mx  ? cudaLaunchKernelEx(&cfg, fused_small_m_kernel<true, false, true>, q)
+      : p.fp8 ? cudaLaunchKernelEx(&cfg, fused_small_m_kernel<true, false, false>, q)
+              : cudaLaunchKernelEx(&cfg, fused_small_m_kernel<false, false, false>, q);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -14,6 +14,13 @@ constexpr int kBlockK = 64;       // K elements per pipeline stage (128 B rows, 
 constexpr int kBlockK8 = 128;     // the same 128-byte rows for one-byte (FP8 E4M3) elements
 constexpr int kTileM = 128;       // tokens per large-M tile (MMA M)
 constexpr int kThreads = 192;     // 6 warps: TMA producer, MMA issuer, 4 epilogue warps
+// Block-scaled FP8: one UE8M0 scale per 32 K values; a 128-row x 4-group
+// scale block is 512 bytes. Per 128-deep K slice a packed weight tile has two
+// blocks (gate, up) and an activation chunk of 128 rows has one.
+constexpr int kMxGroup = 32;
+constexpr int kSfBlockBytes = 512;
+constexpr int kSfStageBytes = 3 * kSfBlockBytes;  // gate + up weight scales, activation scales
+constexpr int kSfTmemCols = 16;                   // TMEM columns per stage of scales (12 used)
 
 struct LargeMParams {
   CUtensorMap tmap_a;  // A  [M, K]       box {64, 128}, 128-B swizzle
@@ -27,9 +34,13 @@ struct LargeMParams {
   float scale_gate, scale_up;  // scale_a * scale_w1 and scale_a * scale_w2 in the epilogue
   int down;  // down-projection (pair kernel): tiles of 256 output columns, out = acc + residual
   const void* residual;  // [M, N] bf16 or null (down-projection only)
+  int mx;    // block-scaled E4M3 (pair kernel): scales from tmap_sw / tmap_sa
+  CUtensorMap tmap_sw;   // weight scales: uint8 rows of 256 bytes, 4 rows (1 KB) per packed tile
+  CUtensorMap tmap_sa;   // activation scales: uint8 rows of 256 bytes, 2 rows per 512-byte block
   uint32_t* status;
   uint64_t timeout_ns;
   int inject_stall;
+  int l2_prefetch;  // single-CTA kernel: K slices of its first tile each CTA stages in L2
 };
 
 struct SmallMParams {
@@ -47,6 +58,9 @@ struct SmallMParams {
   int down;    // down-projection: a block is 256 output columns (rows 0-127 and 128-255
                // of the packed tile), out = acc + residual instead of SiLU(g) * u
   const void* residual;  // [M, N] bf16 or null (down-projection only)
+  int mx;      // block-scaled E4M3 (with fp8): per-stage scales from tmap_sw / tmap_sa
+  CUtensorMap tmap_sw;   // weight scales: uint8 rows of 256 bytes, 4 rows (1 KB) per packed tile
+  CUtensorMap tmap_sa;   // activation scales: uint8 rows of 256 bytes, 2 rows per 512-byte block
   uint32_t* status;
   uint64_t timeout_ns;
   int inject_stall;
@@ -58,6 +72,10 @@ cudaError_t configure_large_m();
 cudaError_t configure_small_m();
 
 int large_m_stages(int bn);
+// K slices of its first tile a single-CTA kernel CTA stages in L2 before its
+// grid-dependency wait: about 64 MB of packed weight over the grid
+// (SWIGLU_L2_PREFETCH_LARGE=n forces n; 0 turns it off).
+int large_m_l2_prefetch(int grid, int bn);
 size_t large_m_smem_bytes(int bn);
 cudaError_t launch_large_m(const LargeMParams& p, cudaStream_t stream);
 
@@ -80,8 +98,9 @@ constexpr int kStatusWords = 4;
 // Device address of that array on the current device (no allocation).
 cudaError_t static_scratch_address(uint32_t** out);
 
-// Pipeline depth of the decode kernel when `ctas_per_sm` CTAs share an SM.
-int small_m_stages(int mt, int ctas_per_sm);
+// Pipeline depth of the decode kernel when `ctas_per_sm` CTAs share an SM;
+// `extra` bytes of scales per stage (block-scaled FP8).
+int small_m_stages(int mt, int ctas_per_sm, int extra = 0);
 
 // Programmatic dependent launch for the fused kernels (on unless the
 // environment sets SWIGLU_PDL=0): a launch may begin while the previous grid
@@ -90,7 +109,7 @@ bool pdl_enabled();
 // Packed weight tiles each decode CTA stages in L2 ahead of its pipeline, for
 // a grid of `grid` CTAs in clusters of `splits` (SWIGLU_L2_PREFETCH=n forces n).
 int small_m_l2_prefetch(int grid, int splits);
-size_t small_m_smem_bytes(int mt, int stages);
+size_t small_m_smem_bytes(int mt, int stages, int extra = 0);
 cudaError_t launch_small_m(const SmallMParams& p, cudaStream_t stream);
 // Clusters of `splits` decode CTAs (shared memory at the 1-CTA-per-SM limit)
 // that can be resident at once; 0 if such clusters cannot be launched.
@@ -100,6 +119,12 @@ cudaError_t launch_pack(const void* w1, const void* w2, void* wp, int K, int N,
                         cudaStream_t stream);
 cudaError_t launch_pack_fp8(const void* w1, const void* w2, void* wp, int K, int N,
                             cudaStream_t stream);
+// Block-scaled FP8 scales: W1's and W2's [K/32, N] -> 1 KB per packed tile;
+// A's [M, K/32] -> 512-byte blocks [ceil(M/128)][ceil(K/128)].
+cudaError_t launch_pack_mx_weight_scales(const void* s1, const void* s2, void* out, int K, int N,
+                                         cudaStream_t stream);
+cudaError_t launch_tile_mx_act_scales(const void* sa, void* out, int M, int K,
+                                      cudaStream_t stream);
 // Down-projection weight W3 [N, H] -> tiles of 256 output columns x 64 K values.
 cudaError_t launch_pack_down(const void* w3, void* wp, int N, int H, cudaStream_t stream);
 

@@ -67,6 +67,41 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Scales of block-scaled FP8 (one byte per 32 K values) in 512-byte blocks
+// of 128 rows x 4 groups: row r, group g at (r % 32) * 16 + (r / 32) * 4 + g;
+// 127 (a scale of 1) where no value exists.
+__device__ __forceinline__ int sf_offset(int r, int g) { return (r & 31) * 16 + (r >> 5) * 4 + g; }
+
+// W1's and W2's scales [groups, N] -> per packed tile (column block j, K slice
+// b): W1's block for columns 128 j + r, groups 4 b + g, then W2's block.
+__global__ void __launch_bounds__(256)
+    pack_mx_weight_scales_kernel(const uint8_t* __restrict__ s1, const uint8_t* __restrict__ s2,
+                                 uint8_t* __restrict__ out, int groups, int N, int k_slices) {
+  const int b = blockIdx.x, j = blockIdx.y;
+  uint8_t* __restrict__ dst = out + (static_cast<size_t>(j) * k_slices + b) * (2 * kSfBlockBytes);
+  for (int idx = threadIdx.x; idx < 2 * kSfBlockBytes; idx += blockDim.x) {
+    const int h = idx / kSfBlockBytes, r = (idx % kSfBlockBytes) >> 2, g = idx & 3;
+    const int n = j * kPackBlockN + r, kg = b * 4 + g;
+    const uint8_t* __restrict__ src = h ? s2 : s1;
+    dst[h * kSfBlockBytes + sf_offset(r, g)] =
+        (n < N && kg < groups) ? src[static_cast<size_t>(kg) * N + n] : uint8_t(127);
+  }
+}
+
+// A's scales [M, groups] -> blocks [ceil(M/128)][k_slices]; grid (row blocks, K slices).
+__global__ void __launch_bounds__(256)
+    tile_mx_act_scales_kernel(const uint8_t* __restrict__ sa, uint8_t* __restrict__ out, int M,
+                              int groups, int k_slices) {
+  const int i = blockIdx.x, b = blockIdx.y;
+  uint8_t* __restrict__ dst = out + (static_cast<size_t>(i) * k_slices + b) * kSfBlockBytes;
+  for (int idx = threadIdx.x; idx < kSfBlockBytes; idx += blockDim.x) {
+    const int r = idx >> 2, g = idx & 3;
+    const int m = i * 128 + r, kg = b * 4 + g;
+    dst[sf_offset(r, g)] =
+        (m < M && kg < groups) ? sa[static_cast<size_t>(m) * groups + kg] : uint8_t(127);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_pack_down(const void* w3, void* wp, int N, int H, cudaStream_t stream) {
@@ -96,6 +131,26 @@ cudaError_t launch_pack_fp8(const void* w1, const void* w2, void* wp, int K, int
   pack_kernel<uint8_t, kBlockK8><<<grid, 256, 0, stream>>>(
       static_cast<const uint8_t*>(w1), static_cast<const uint8_t*>(w2),
       static_cast<uint8_t*>(wp), K, N, k_slices);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_mx_weight_scales(const void* s1, const void* s2, void* out, int K, int N,
+                                         cudaStream_t stream) {
+  const int n_blocks = (N + kPackBlockN - 1) / kPackBlockN;
+  const int k_slices = (K + kBlockK8 - 1) / kBlockK8;
+  pack_mx_weight_scales_kernel<<<dim3(k_slices, n_blocks), 256, 0, stream>>>(
+      static_cast<const uint8_t*>(s1), static_cast<const uint8_t*>(s2), static_cast<uint8_t*>(out),
+      (K + kMxGroup - 1) / kMxGroup, N, k_slices);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tile_mx_act_scales(const void* sa, void* out, int M, int K,
+                                      cudaStream_t stream) {
+  const int m_blocks = (M + 127) / 128;
+  const int k_slices = (K + kBlockK8 - 1) / kBlockK8;
+  tile_mx_act_scales_kernel<<<dim3(m_blocks, k_slices), 256, 0, stream>>>(
+      static_cast<const uint8_t*>(sa), static_cast<uint8_t*>(out), M, (K + kMxGroup - 1) / kMxGroup,
+      k_slices);
   return cudaGetLastError();
 }
 

@@ -160,6 +160,14 @@ __device__ __forceinline__ void tma_prefetch_l2_3d_hint(const CUtensorMap* map, 
       : "memory");
 }
 
+// Bring one 2-D tile into L2 (no destination, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t c0, int32_t c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+
 // 2-D tiled load global -> shared; completion counted in bytes on `bar`.
 // c0 is the innermost (contiguous) coordinate; it is always a multiple of 64
 // elements here (128 bytes), so the 16-byte rule for TMA holds.
@@ -299,6 +307,54 @@ __device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint6
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// --------------------------------------- block-scaled FP8 (kind::mxf8f6f4) ---
+// Scale factors live in tensor memory. One 512-byte block in shared memory
+// holds one-byte scales for 128 rows x 4 groups of 32 K values, row r / group
+// g at byte (r % 32) * 16 + (r / 32) * 4 + g, i.e. 32 lines of 16 bytes.
+// tcgen05.cp .32x128b.warpx4 copies those 32 lines into 4 consecutive TMEM
+// columns of every 32-lane quarter, so lane 32q + (r % 32), column r / 32
+// holds the four group scales of row r; an MMA's scale-factor ID (0..3) picks
+// the byte of the group it consumes (one MMA covers K = 32: one group).
+
+// Descriptor of a 512-byte scale block: no swizzle, 8-line core matrices of
+// 128 bytes stacked contiguously (both byte offsets 128), version 1.
+__device__ __forceinline__ uint64_t smem_desc_sf(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(128 >> 4) << 16) |
+         (static_cast<uint64_t>(128 >> 4) << 32) | (static_cast<uint64_t>(1) << 46);
+}
+
+__device__ __forceinline__ void tmem_cp_sf(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc)
+               : "memory");
+}
+
+// CTA-pair form, issued by the even CTA: each CTA copies the block at this
+// shared-memory offset of its own shared memory into its own tensor memory.
+__device__ __forceinline__ void tmem_cp_sf_pair(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc)
+               : "memory");
+}
+
+// Instruction descriptor, kind::mxf8f6f4, E4M3 A and B (format 0), K-major,
+// N >> 3 at bits 17-22, scale type UE8M0 (bit 23), M >> 4 at bits 24-28, and
+// the scale-factor byte IDs of B (bits 4-5) and A (bits 29-30).
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(int m, int n, int sf_id) {
+  return (static_cast<uint32_t>(sf_id) << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) |
+         (static_cast<uint32_t>(m >> 4) << 24) | (static_cast<uint32_t>(sf_id) << 29);
+}
+
+// D[tmem] (+)= (A .* scaleA) * (B .* scaleB)^T over K = 32, scales from TMEM.
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
 
@@ -462,6 +518,17 @@ __device__ __forceinline__ void mma_e4m3_pair(uint32_t d_tmem, uint64_t a_desc, 
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_mx_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
 

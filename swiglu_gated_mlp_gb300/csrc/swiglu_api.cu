@@ -80,6 +80,13 @@ int small_m_l2_prefetch(int grid, int splits) {
   const int64_t per_tile = 2 * int64_t(kPackBlockN) * 128;  // one packed tile: 32 KB
   return static_cast<int>(std::clamp<int64_t>(budget / (int64_t(std::max(grid, 1)) * per_tile), 2, 16));
 }
+int large_m_l2_prefetch(int grid, int bn) {
+  static const int64_t forced = env_int("SWIGLU_L2_PREFETCH_LARGE", -1);
+  if (forced >= 0) return static_cast<int>(std::min<int64_t>(forced, 1 << 20));
+  const int64_t budget = int64_t(64) << 20;
+  const int64_t per_slice = 2 * int64_t(bn) * 128;  // gate and up rows of one 64-deep K slice
+  return static_cast<int>(budget / (int64_t(std::max(grid, 1)) * per_slice));
+}
 }  // namespace swg
 
 namespace {
@@ -484,6 +491,7 @@ swiglu_status_t launch_forward(const void* A, const void* Wp, void* Y, int64_t M
     p.status = d.status;
     p.timeout_ns = timeout;
     p.inject_stall = inject;
+    if (pl.variant == SWIGLU_VARIANT_LARGE_M) p.l2_prefetch = swg::large_m_l2_prefetch(pl.grid, pl.bn);
     err = pl.variant == SWIGLU_VARIANT_LARGE_M_PAIR ? swg::launch_large_m_pair(p, stream)
           : pl.variant == SWIGLU_VARIANT_SEQUENTIAL ? swg::launch_sequential(p, stream)
                                                     : swg::launch_large_m(p, stream);
@@ -584,6 +592,41 @@ bool fp8_uses_decode(int64_t M, int64_t N, const DeviceState& d) {
   const int64_t nb = padded_n(N) / swg::kPackBlockN;
   return M <= 32 || (M <= 64 && nb * 2 <= d.sm_count) ||
          (M <= 80 && nb <= d.sm_count && nb * 2 > d.sm_count) || d.max_pairs < 1;
+}
+
+// Scale bytes of the block-scaled packed weight: 1 KB per (column block, K slice) tile.
+size_t mx_weight_scale_bytes(int64_t K, int64_t N) {
+  return size_t(padded_n(N) / swg::kPackBlockN) * size_t(k_slices8(K)) * 2 * swg::kSfBlockBytes;
+}
+
+// The block-scaled forward's kernel and launch shape: the decode kernel by the
+// FP8 rule, with all tokens in one group (a scale block holds 128 rows from
+// token 0, so M <= 128), the ring sized with the scales, and K split over
+// clusters on narrow N as for the other forms; CTA pairs otherwise.
+swiglu_status_t make_mx_plan(int64_t M, int64_t K, int64_t N, const DeviceState& d, Plan* pl) {
+  const int64_t kslices = k_slices8(K);
+  if (M > 128 || !fp8_uses_decode(M, N, d)) {
+    if (d.max_pairs < 1) return SWIGLU_ERR_UNSUPPORTED;
+    return make_plan(M, K, N, SWIGLU_VARIANT_LARGE_M_PAIR, &d, pl, 1);
+  }
+  *pl = Plan{};
+  pl->variant = SWIGLU_VARIANT_SMALL_M;
+  pl->tiles = static_cast<int>(padded_n(N) / swg::kPackBlockN);
+  pl->mt = static_cast<int>((M + 15) / 16 * 16);
+  pl->mgroups = 1;
+  pl->stages = swg::small_m_stages(pl->mt, 1, swg::kSfStageBytes);
+  pl->splits = 1;
+  const int64_t stage_bytes = 2 * swg::kPackBlockN * swg::kBlockK * 2 + int64_t(pl->mt) * 128;
+  if (int64_t(pl->mt) * 1024 <= pl->stages * stage_bytes) {
+    for (int s : {8, 4, 2}) {
+      if (int64_t(pl->tiles) * s <= d.sm_count && s <= kslices && d.small_clusters[s] >= pl->tiles) {
+        pl->splits = s;
+        break;
+      }
+    }
+  }
+  pl->grid = pl->tiles * pl->splits;
+  return SWIGLU_OK;
 }
 }  // namespace
 
@@ -885,6 +928,175 @@ swiglu_status_t swiglu_forward_fp8(const void* A, const void* Wpacked, void* Y, 
     p.fp8 = 1;
     p.scale_gate = sg;
     p.scale_up = su;
+    p.status = d->status;
+    p.timeout_ns = g_timeout_ns.load();
+    p.inject_stall = g_inject.load();
+    err = swg::launch_large_m_pair(p, cs);
+  }
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_ERR_CUDA;
+  }
+  return SWIGLU_OK;
+}
+
+size_t swiglu_packed_weight_bytes_mxfp8(int64_t K, int64_t N) {
+  const size_t values = swiglu_packed_weight_bytes_fp8(K, N);
+  if (values == 0) return 0;
+  return values + mx_weight_scale_bytes(K, N);
+}
+
+size_t swiglu_act_scale_bytes_mxfp8(int64_t M, int64_t K) {
+  if (M < 0 || K <= 0 || M > kMaxM || K > kMaxKN) return 0;
+  return size_t((M + 127) / 128) * size_t(k_slices8(K)) * swg::kSfBlockBytes;
+}
+
+swiglu_status_t swiglu_pack_weights_mxfp8(const void* W1, const void* S1, const void* W2,
+                                          const void* S2, void* Wpacked, int64_t K, int64_t N,
+                                          swiglu_stream_t stream) {
+  swiglu_status_t st = check_shape(0, K, N);
+  if (st != SWIGLU_OK) return st;
+  if ((K % swg::kMxGroup) != 0) return SWIGLU_ERR_UNSUPPORTED;  // whole scale groups
+  if (!W1 || !W2 || !S1 || !S2 || !Wpacked) return SWIGLU_ERR_INVALID_ARG;
+  if (!aligned16(W1) || !aligned16(W2) || !aligned16(Wpacked)) return SWIGLU_ERR_INVALID_ARG;
+  const size_t w_bytes = size_t(K) * size_t(N), s_bytes = size_t(K / swg::kMxGroup) * size_t(N);
+  const size_t p_bytes = swiglu_packed_weight_bytes_mxfp8(K, N);
+  if (overlaps(Wpacked, p_bytes, W1, w_bytes) || overlaps(Wpacked, p_bytes, W2, w_bytes) ||
+      overlaps(Wpacked, p_bytes, S1, s_bytes) || overlaps(Wpacked, p_bytes, S2, s_bytes))
+    return SWIGLU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != SWIGLU_OK) return st;
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* scales = static_cast<uint8_t*>(Wpacked) + swiglu_packed_weight_bytes_fp8(K, N);
+  if (swg::launch_pack_fp8(W1, W2, Wpacked, static_cast<int>(K), static_cast<int>(N), cs) !=
+          cudaSuccess ||
+      swg::launch_pack_mx_weight_scales(S1, S2, scales, static_cast<int>(K), static_cast<int>(N),
+                                        cs) != cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_ERR_CUDA;
+  }
+  return SWIGLU_OK;
+}
+
+swiglu_status_t swiglu_pack_act_scales_mxfp8(const void* SA, void* SAtiled, int64_t M, int64_t K,
+                                             swiglu_stream_t stream) {
+  swiglu_status_t st = check_shape(M, K, 8);
+  if (st != SWIGLU_OK) return st;
+  if ((K % swg::kMxGroup) != 0) return SWIGLU_ERR_UNSUPPORTED;
+  if (M == 0) return SWIGLU_OK;
+  if (!SA || !SAtiled || !aligned16(SAtiled)) return SWIGLU_ERR_INVALID_ARG;
+  if (overlaps(SAtiled, swiglu_act_scale_bytes_mxfp8(M, K), SA,
+               size_t(M) * size_t(K / swg::kMxGroup)))
+    return SWIGLU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != SWIGLU_OK) return st;
+  if (swg::launch_tile_mx_act_scales(SA, SAtiled, static_cast<int>(M), static_cast<int>(K),
+                                     reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_ERR_CUDA;
+  }
+  return SWIGLU_OK;
+}
+
+swiglu_status_t swiglu_plan_string_mxfp8(int64_t M, int64_t K, int64_t N, char* buf,
+                                         size_t buflen) {
+  if (!buf || buflen == 0) return SWIGLU_ERR_INVALID_ARG;
+  buf[0] = '\0';
+  swiglu_status_t st = check_shape(M, K, N);
+  if (st != SWIGLU_OK) return st;
+  if ((K % swg::kMxGroup) != 0) return SWIGLU_ERR_UNSUPPORTED;
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != SWIGLU_OK) return st;
+  Plan pl;
+  st = make_mx_plan(M < 1 ? 1 : M, K, N, *d, &pl);
+  if (st != SWIGLU_OK) return st;
+  format_plan(pl, *d, "mxfp8 ", buf, buflen);
+  return SWIGLU_OK;
+}
+
+swiglu_status_t swiglu_forward_mxfp8(const void* A, const void* SAtiled, const void* Wpacked,
+                                     void* Y, int64_t M, int64_t K, int64_t N,
+                                     swiglu_stream_t stream) {
+  swiglu_status_t st = check_shape(M, K, N);
+  if (st != SWIGLU_OK) return st;
+  if ((K % swg::kMxGroup) != 0) return SWIGLU_ERR_UNSUPPORTED;
+  if (M == 0) return SWIGLU_OK;
+  if (!A || !SAtiled || !Wpacked || !Y) return SWIGLU_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(SAtiled) || !aligned16(Wpacked) || !aligned16(Y))
+    return SWIGLU_ERR_INVALID_ARG;
+  const size_t a_bytes = size_t(M) * size_t(K), y_bytes = size_t(M) * size_t(N) * 2;
+  if (overlaps(Y, y_bytes, A, a_bytes) ||
+      overlaps(Y, y_bytes, Wpacked, swiglu_packed_weight_bytes_mxfp8(K, N)) ||
+      overlaps(Y, y_bytes, SAtiled, swiglu_act_scale_bytes_mxfp8(M, K)))
+    return SWIGLU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != SWIGLU_OK) return st;
+  Plan pl;
+  st = make_mx_plan(M, K, N, *d, &pl);
+  if (st != SWIGLU_OK) return st;
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  // scale tensors as rows of 256 bytes: 4 rows per packed weight tile, 2 rows
+  // per activation block of 128 rows x one 128-deep K slice
+  const uint8_t* wscales = static_cast<const uint8_t*>(Wpacked) + swiglu_packed_weight_bytes_fp8(K, N);
+  const uint64_t w_rows = uint64_t(padded_n(N) / swg::kPackBlockN) * uint64_t(k_slices8(K)) * 4;
+  const uint64_t a_rows = uint64_t((M + 127) / 128) * uint64_t(k_slices8(K)) * 2;
+  CUtensorMap tmap_sw, tmap_sa;
+  if (!encode_2d(&tmap_sw, wscales, 256, w_rows, 256, 256, 4, CU_TENSOR_MAP_SWIZZLE_NONE,
+                 CU_TENSOR_MAP_DATA_TYPE_UINT8) ||
+      !encode_2d(&tmap_sa, SAtiled, 256, a_rows, 256, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE,
+                 CU_TENSOR_MAP_DATA_TYPE_UINT8))
+    return SWIGLU_ERR_CUDA;
+  cudaError_t err;
+  if (pl.variant == SWIGLU_VARIANT_SMALL_M) {
+    swg::SmallMParams p{};
+    if (!encode_2d(&p.tmap_x, A, K, M, K, swg::kBlockK8, pl.mt, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_DATA_TYPE_UINT8) ||
+        !encode_packed_w8(&p.tmap_w, Wpacked, K, N, 2 * swg::kPackBlockN))
+      return SWIGLU_ERR_CUDA;
+    p.tmap_sw = tmap_sw;
+    p.tmap_sa = tmap_sa;
+    p.y = Y;
+    p.M = static_cast<int>(M);
+    p.K = static_cast<int>(K);
+    p.N = static_cast<int>(N);
+    p.mt = pl.mt;
+    p.stages = pl.stages;
+    p.grid = pl.grid;
+    p.splits = pl.splits;
+    p.mgroups = pl.mgroups;
+    p.fp8 = 1;
+    p.mx = 1;
+    p.scale_gate = 1.0f;  // the scales act inside the MMA
+    p.scale_up = 1.0f;
+    p.status = d->status;
+    p.timeout_ns = g_timeout_ns.load();
+    p.inject_stall = g_inject.load();
+    err = swg::launch_small_m(p, cs);
+  } else {
+    swg::LargeMParams p{};
+    if (!encode_2d(&p.tmap_a, A, K, M, K, swg::kBlockK8, swg::kTileM, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_DATA_TYPE_UINT8) ||
+        !encode_packed_w8(&p.tmap_w, Wpacked, K, N, pl.bn) ||
+        !encode_2d(&p.tmap_y, Y, N, M, N * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+      return SWIGLU_ERR_CUDA;
+    p.tmap_sw = tmap_sw;
+    p.tmap_sa = tmap_sa;
+    p.M = static_cast<int>(M);
+    p.K = static_cast<int>(K);
+    p.N = static_cast<int>(N);
+    p.tiles_m = pl.tiles_m;
+    p.tiles_n = pl.tiles_n;
+    p.group_m = pl.group_m;
+    p.bn = pl.bn;
+    p.grid = pl.grid;
+    p.fp8 = 1;
+    p.mx = 1;
+    p.scale_gate = 1.0f;
+    p.scale_up = 1.0f;
     p.status = d->status;
     p.timeout_ns = g_timeout_ns.load();
     p.inject_stall = g_inject.load();

@@ -126,3 +126,27 @@ def test_binding_rejects_cpu_tensors(native_lib):
         native_lib.swiglu_forward(a, a, 64)
     with pytest.raises(ValueError):
         native_lib.swiglu_pack_weights(a, a)
+
+
+def test_block_scaled_sizes(native_lib):
+    f = native_lib.swiglu_packed_weight_bytes_mxfp8
+    # values as the per-tensor FP8 layout, then 1 KB of scales per 32 KB tile
+    assert f(128, 128) == 2 * 128 * 128 + 1024
+    assert f(160, 136) == 2 * 256 * 256 + 4 * 1024     # Np = 256, Kp = 256: 4 tiles
+    assert f(0, 128) == 0
+    g = native_lib.swiglu_act_scale_bytes_mxfp8
+    assert g(128, 128) == 512 and g(129, 128) == 1024 and g(1, 160) == 1024
+    assert g(0, 128) == 0 and g(5, 0) == 0
+
+
+def test_block_scaled_argument_checks(native_lib):
+    lib = native_lib.lib
+    # K not a multiple of 32 (the scale group): UNSUPPORTED before any device work
+    assert lib.swiglu_forward_mxfp8(FAKE, FAKE, FAKE, FAKE * 64, 4, 48, 64, None) == 2
+    assert lib.swiglu_pack_weights_mxfp8(FAKE, FAKE, FAKE, FAKE, FAKE * 64, 48, 64, None) == 2
+    assert lib.swiglu_pack_act_scales_mxfp8(FAKE, FAKE * 4, 4, 48, None) == 2
+    # null scale pointer, misaligned block scales: INVALID_ARG
+    assert lib.swiglu_forward_mxfp8(FAKE, None, FAKE, FAKE * 64, 4, 64, 64, None) == 1
+    assert lib.swiglu_forward_mxfp8(FAKE, FAKE + 8, FAKE * 16, FAKE * 64, 4, 64, 64, None) == 1
+    # M = 0 is a no-op
+    assert lib.swiglu_forward_mxfp8(FAKE, FAKE, FAKE, FAKE, 0, 64, 64, None) == 0

@@ -63,10 +63,12 @@ def test_fp8_forward_matches_oracle(native, M, K, N):
     run_fp8(native, M, K, N, seed=M + 3 * K + N)
 
 
-@pytest.mark.parametrize("name", ["qwen2.5-7b-decode-m16", "qwen2.5-7b-prefill-m4096"])
+@pytest.mark.parametrize("name", ["qwen2.5-7b-decode-m16", "qwen2.5-7b-prefill-m4096",
+                                  "qwen2.5-72b-prefill-m8192"])
 def test_fp8_full_size_workloads(native, name):
+    # 512 sampled rows (0 and M-1 included) x every column, as for bf16
     w = WORKLOADS[name]
-    rows = sample_rows(w.M, 64, seed=w.seed)
+    rows = sample_rows(w.M, 512, seed=w.seed)
     rep = run_fp8(native, w.M, w.K, w.N, seed=w.seed, rows=rows)
     assert rep["mismatch_rate"] == 0.0
 
