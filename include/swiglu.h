@@ -82,8 +82,11 @@ typedef enum {
   SWIGLU_VARIANT_LARGE_M = 1, /* 128-token tiles of A, weight columns as the MMA N side */
   SWIGLU_VARIANT_SMALL_M = 2, /* weights as the MMA M side, tokens as N (M <= 256) */
   SWIGLU_VARIANT_LARGE_M_PAIR = 3, /* 256-token tiles on CTA pairs (tcgen05 cta_group::2) */
-  SWIGLU_VARIANT_SEQUENTIAL = 4    /* gate K loop, then up K loop with SiLU(gate) computed
+  SWIGLU_VARIANT_SEQUENTIAL = 4,   /* gate K loop, then up K loop with SiLU(gate) computed
                                       meanwhile: the pages' Kernel-1 schedule, for comparison */
+  SWIGLU_VARIANT_SPLIT_K = 5       /* 128 x 64 output tiles, each on a cluster of 2 CTAs that
+                                      split K and sum their halves in shared memory (small
+                                      single-wave problems) */
 } swiglu_variant_t;
 
 /*

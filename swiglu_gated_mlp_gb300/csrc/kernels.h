@@ -26,6 +26,7 @@ struct LargeMParams {
   CUtensorMap tmap_a;  // A  [M, K]       box {64, 128}, 128-B swizzle
   CUtensorMap tmap_w;  // Wp {64, 256, tiles} box {64, bn, 1}, 128-B swizzle
   CUtensorMap tmap_y;  // Y  [M, N]       box {32, 32},  64-B swizzle (store)
+  void* y;             // Y [M, N] bf16 (split-K kernel: plain row stores)
   int M, K, N;
   int tiles_m, tiles_n, group_m;
   int bn;    // output columns per tile: 32, 64 or 128 (MMA N = 2 * bn)
@@ -85,6 +86,13 @@ cudaError_t configure_large_m_pair(int* max_pairs);
 size_t large_m_pair_smem_bytes();
 int large_m_pair_stages();
 cudaError_t launch_large_m_pair(const LargeMParams& p, cudaStream_t stream);
+
+// K split over the two CTAs of a cluster, one 128 x 64 output tile per cluster
+// (grid = 2 x tiles): single-wave problems whose tiles need more operand bytes
+// than one SM's shared memory holds.
+cudaError_t configure_split_k(int* max_clusters);
+int split_k_bn();
+cudaError_t launch_split_k(const LargeMParams& p, cudaStream_t stream);
 
 // Sequential gate-then-up schedule (bn = 128, 128-row tiles), an ablation.
 cudaError_t configure_sequential();

@@ -26,6 +26,7 @@ struct DeviceState {
   int sm_count = 0;
   int max_pairs = 0;           // CTA pairs of the pair kernel resident at once
   int small_clusters[9] = {};  // decode-kernel clusters of s CTAs resident at once (s = 2, 4, 8)
+  int split_clusters = 0;      // split-K kernel clusters (of 2) resident at once
   uint32_t* status = nullptr;  // uint32_t[4], see ptx.cuh
 };
 
@@ -132,10 +133,14 @@ swiglu_status_t init_device(int dev, DeviceState& d) {
     return SWIGLU_ERR_CUDA;
   }
   for (int s : {2, 4, 8}) d.small_clusters[s] = swg::small_m_max_clusters(s);
-  // The CTA-pair kernel is optional: if its set-up fails, that variant is unavailable.
+  // The CTA-pair and split-K kernels are optional: if a set-up fails, that variant is unavailable.
   if (swg::configure_large_m_pair(&d.max_pairs) != cudaSuccess) {
     cudaGetLastError();
     d.max_pairs = 0;
+  }
+  if (swg::configure_split_k(&d.split_clusters) != cudaSuccess) {
+    cudaGetLastError();
+    d.split_clusters = 0;
   }
   return SWIGLU_OK;
 }
@@ -337,8 +342,11 @@ swiglu_status_t make_plan(int64_t M, int64_t K, int64_t N, int variant, const De
   const int64_t kslices = elem_bytes == 1 ? k_slices8(K) : k_slices(K);
   const int sm_count = d ? d->sm_count : 0;
   const int max_pairs = d ? d->max_pairs : 0;
-  if (variant < SWIGLU_VARIANT_AUTO || variant > SWIGLU_VARIANT_SEQUENTIAL)
+  const int split_clusters = d ? d->split_clusters : 0;
+  if (variant < SWIGLU_VARIANT_AUTO || variant > SWIGLU_VARIANT_SPLIT_K)
     return SWIGLU_ERR_INVALID_ARG;
+  const int64_t split_bn = swg::split_k_bn();
+  const int64_t split_tiles = ((M + swg::kTileM - 1) / swg::kTileM) * ((N + split_bn - 1) / split_bn);
   if (variant == SWIGLU_VARIANT_AUTO) {
     const int64_t nb = padded_n(N) / swg::kPackBlockN;
     const int64_t tiles128 = ((M + swg::kTileM - 1) / swg::kTileM) * nb;
@@ -369,6 +377,18 @@ swiglu_status_t make_plan(int64_t M, int64_t K, int64_t N, int variant, const De
     // whole grid resident; with few units, K splits over clusters.
     decode_split_plan(M, pl->tiles, kslices, d, &pl->mt, &pl->mgroups, &pl->stages, &pl->splits);
     pl->grid = pl->tiles * pl->mgroups * pl->splits;
+    return SWIGLU_OK;
+  }
+  if (variant == SWIGLU_VARIANT_SPLIT_K) {
+    if (split_clusters < 1 || elem_bytes != 2) return SWIGLU_ERR_UNSUPPORTED;
+    if (split_tiles > 1073741823) return SWIGLU_ERR_UNSUPPORTED;
+    pl->bn = static_cast<int>(split_bn);
+    pl->stages = 7;
+    pl->tiles_m = static_cast<int>((M + swg::kTileM - 1) / swg::kTileM);
+    pl->tiles_n = static_cast<int>((N + split_bn - 1) / split_bn);
+    pl->group_m = 1;
+    pl->tiles = static_cast<int>(split_tiles);
+    pl->grid = 2 * pl->tiles;
     return SWIGLU_OK;
   }
   if (variant == SWIGLU_VARIANT_SEQUENTIAL) {
@@ -480,6 +500,7 @@ swiglu_status_t launch_forward(const void* A, const void* Wp, void* Y, int64_t M
         !encode_packed_w(&p.tmap_w, Wp, K, N, pl.bn) ||
         !encode_2d(&p.tmap_y, Y, N, M, N * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
       return SWIGLU_ERR_CUDA;
+    p.y = Y;
     p.M = static_cast<int>(M);
     p.K = static_cast<int>(K);
     p.N = static_cast<int>(N);
@@ -494,6 +515,7 @@ swiglu_status_t launch_forward(const void* A, const void* Wp, void* Y, int64_t M
     if (pl.variant == SWIGLU_VARIANT_LARGE_M) p.l2_prefetch = swg::large_m_l2_prefetch(pl.grid, pl.bn);
     err = pl.variant == SWIGLU_VARIANT_LARGE_M_PAIR ? swg::launch_large_m_pair(p, stream)
           : pl.variant == SWIGLU_VARIANT_SEQUENTIAL ? swg::launch_sequential(p, stream)
+          : pl.variant == SWIGLU_VARIANT_SPLIT_K    ? swg::launch_split_k(p, stream)
                                                     : swg::launch_large_m(p, stream);
   }
   if (err != cudaSuccess) {
@@ -575,6 +597,9 @@ void format_plan(const Plan& pl, const DeviceState& d, const char* prefix, char*
   else if (pl.variant == SWIGLU_VARIANT_SEQUENTIAL)
     std::snprintf(buf, buflen, "%ssequential bn=%d stages=%d tiles=%d grid=%d group_m=%d sms=%d",
                   prefix, pl.bn, pl.stages, pl.tiles, pl.grid, pl.group_m, d.sm_count);
+  else if (pl.variant == SWIGLU_VARIANT_SPLIT_K)
+    std::snprintf(buf, buflen, "%ssplit_k bn=%d stages=%d tiles=%d grid=%d clusters=%d sms=%d",
+                  prefix, pl.bn, pl.stages, pl.tiles, pl.grid, d.split_clusters, d.sm_count);
   else if (pl.variant == SWIGLU_VARIANT_LARGE_M_PAIR)
     std::snprintf(buf, buflen,
                   "%slarge_m_pair bn=%d stages=%d tiles=%d grid=%d group_m=%d max_pairs=%d sms=%d",
@@ -663,7 +688,7 @@ swiglu_status_t swiglu_forward_variant(const void* A, const void* Wpacked, void*
                                        swiglu_stream_t stream) {
   swiglu_status_t st = check_forward_args(A, Wpacked, Y, M, K, N);
   if (st != SWIGLU_OK) return st;
-  if (variant < SWIGLU_VARIANT_AUTO || variant > SWIGLU_VARIANT_SEQUENTIAL)
+  if (variant < SWIGLU_VARIANT_AUTO || variant > SWIGLU_VARIANT_SPLIT_K)
     return SWIGLU_ERR_INVALID_ARG;
   if (M == 0) return SWIGLU_OK;
   DeviceState* d = nullptr;

@@ -18,7 +18,7 @@ from gpu_helpers import (check_against_oracle, run_forward, sentinel_buffer, sen
 
 pytestmark = pytest.mark.gpu
 
-AUTO, LARGE, SMALL, PAIR, SEQ = 0, 1, 2, 3, 4
+AUTO, LARGE, SMALL, PAIR, SEQ, SPLIT = 0, 1, 2, 3, 4, 5
 
 
 @pytest.fixture(scope="module")
@@ -106,6 +106,19 @@ def test_pair_kernel_matches_oracle(native, M, K, N):
     check_against_oracle(native, M, K, N, seed=M * 3 + K + N, variant=PAIR)
 
 
+# K split over the two CTAs of a cluster, one 128 x 64 tile per cluster: the
+# 0.5B shape, ragged K (a CTA with no K slice when K is one slice), ragged N,
+# two row tiles, and a long K loop that wraps the 7-stage ring.
+SPLITK_CASES = [(128, 896, 4864), (100, 200, 264), (1, 64, 128), (129, 136, 256),
+                (300, 512, 1000), (256, 3584, 1024), (90, 8, 8)]
+
+
+@pytest.mark.parametrize("M,K,N", SPLITK_CASES)
+def test_split_k_kernel_matches_oracle(native, M, K, N):
+    assert native.swiglu_plan_string(M, K, N, SPLIT).startswith("split_k"), (M, K, N)
+    check_against_oracle(native, M, K, N, seed=M * 19 + K + N, variant=SPLIT)
+
+
 # The pages' Kernel-1 schedule (gate K loop, then up K loop), kept for comparison.
 SEQ_CASES = [(1, 64, 128), (100, 200, 264), (129, 136, 256), (300, 512, 1000), (513, 896, 4864),
              (2048, 128, 2048)]
@@ -121,7 +134,7 @@ def test_auto_choice_matches_oracle(native, M, K, N):
     check_against_oracle(native, M, K, N, seed=M + K + N, variant=AUTO)
 
 
-@pytest.mark.parametrize("variant", [LARGE, SMALL, PAIR, SEQ])
+@pytest.mark.parametrize("variant", [LARGE, SMALL, PAIR, SEQ, SPLIT])
 def test_variants_agree(native, variant):
     # both kernels accumulate in fp32; their bf16 outputs agree within 1 ulp-ish
     a, w1, w2 = make_inputs(48, 640, 512, seed=77)
@@ -158,7 +171,7 @@ def test_largest_k_and_n_match_oracle(native, M, K, N):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("variant", [AUTO, LARGE, SMALL, PAIR, SEQ])
+@pytest.mark.parametrize("variant", [AUTO, LARGE, SMALL, PAIR, SEQ, SPLIT])
 @pytest.mark.parametrize("M", [1, 9, 130])
 def test_smallest_k_and_n_match_oracle(native, variant, M):
     check_against_oracle(native, M, 8, 8, seed=M + variant, variant=variant)
