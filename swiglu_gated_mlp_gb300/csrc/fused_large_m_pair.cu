@@ -33,32 +33,39 @@
 // (tcgen05.cp.cta_group::2, each CTA from its own shared memory) and issues
 // kind::mxf8f6f4 MMAs. The scale slots take the second half of tensor memory,
 // so the accumulator is single-buffered: the next tile's MMAs wait for the
-// epilogue to have read the previous one.
+// epilogue to have read the previous one. To keep that wait short the
+// block-scaled form runs 8 epilogue warps (two per tensor-memory lane
+// quarter, 64 output columns each) that load their whole share of the
+// accumulator into registers, release it at once, and only then apply
+// SiLU(g) * u and store; its ring is 5 stages deep to make room for their
+// store staging.
 #include "kernels.h"
 #include "ptx.cuh"
 
 namespace swg {
 namespace {
 
+template <bool kMx>
 struct PairCfg {
   static constexpr int kBN = 128;                        // output columns per tile
   static constexpr int kABytes = 128 * kBlockK * 2;      // 16 KB: this CTA's 128 A rows
   static constexpr int kBBytes = 128 * kBlockK * 2;      // 16 KB: this CTA's 128 weight rows
   static constexpr int kStageBytes = kABytes + kBBytes;  // 32 KB per CTA, 64 KB per pair
-  static constexpr int kStages = 6;
+  static constexpr int kStages = kMx ? 5 : 6;
+  static constexpr int kEpiWarps = kMx ? 8 : 4;          // 2 per lane quarter when block-scaled
+  static constexpr int kThreadsT = 64 + 32 * kEpiWarps;  // + TMA producer and MMA issuer warps
   static constexpr int kAccCols = 2 * kBN;               // 256 fp32 columns: gate | up
-  static constexpr int kTmemCols = 2 * kAccCols;         // double buffered
+  static constexpr int kTmemCols = 2 * kAccCols;         // double buffered (bf16, per-tensor FP8)
   static constexpr int kStgBytes = 32 * 32 * 2;          // 32 rows x 64 B store staging
-  static constexpr int kNumStg = 8;
+  static constexpr int kNumStg = 2 * kEpiWarps;
   static constexpr int kBarBytes = 256;
-  static constexpr size_t kSmem =
-      1024 + size_t(kStages) * kStageBytes + size_t(kNumStg) * kStgBytes + kBarBytes;
-  static_assert(kSmem <= 232448, "shared memory budget");
   // block-scaled FP8: 1.5 KB of scales per stage (A block, gate and up weight blocks)
-  static constexpr size_t kSmemMx = kSmem + size_t(kStages) * kSfStageBytes;
-  static_assert(kSmemMx <= 232448, "shared memory budget (block-scaled)");
+  static constexpr size_t kSmem = 1024 + size_t(kStages) * kStageBytes +
+                                  size_t(kNumStg) * kStgBytes +
+                                  (kMx ? size_t(kStages) * kSfStageBytes : 0) + kBarBytes;
+  static_assert(kSmem <= 232448, "shared memory budget");
   static constexpr int kSfCol = kAccCols;  // scale slots after the single accumulator
-  static_assert(kSfCol + kStages * kSfTmemCols <= kTmemCols, "tensor memory budget");
+  static_assert(!kMx || kSfCol + kStages * kSfTmemCols <= kTmemCols, "tensor memory budget");
 };
 
 __device__ __forceinline__ void pair_tile_coords(int t, int tiles_m, int tiles_n, int group_m,
@@ -73,9 +80,9 @@ __device__ __forceinline__ void pair_tile_coords(int t, int tiles_m, int tiles_n
 }
 
 template <bool kFp8, bool kDown, bool kMx>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(PairCfg<kMx>::kThreadsT, 1)
     fused_large_m_pair_kernel(const __grid_constant__ LargeMParams p) {
-  using C = PairCfg;
+  using C = PairCfg<kMx>;
   static_assert(!kMx || (kFp8 && !kDown), "block scales go with E4M3 gate/up inputs");
   constexpr int kAccBufs = kMx ? 1 : 2;  // accumulator buffers in tensor memory
   // K values per stage: 64 bf16 or 128 E4M3, a 128-byte row either way
@@ -124,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull0 + 8u * b, 1);   // multicast MMA commit
-      mbar_init(tempty0 + 8u * b, 8);  // 4 epilogue warps x 2 CTAs (used on rank 0)
+      mbar_init(tempty0 + 8u * b, 2 * C::kEpiWarps);  // epilogue warps x 2 CTAs (used on rank 0)
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -270,7 +277,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + lane_off + buf * C::kAccCols;
-      if constexpr (kDown) {
+      if constexpr (kMx) {
+        // this warp's 64 output columns [64 h, 64 h + 64): gate and up, all loaded
+        // before the accumulator is released to the next tile's MMAs
+        const int h = ew >> 2;
+        uint32_t g0[32], g1[32], u0[32], u1[32];
+        tmem_ld_x32(tacc + 64 * h, g0);
+        tmem_ld_x32(tacc + 64 * h + 32, g1);
+        tmem_ld_x32(tacc + C::kBN + 64 * h, u0);
+        tmem_ld_x32(tacc + C::kBN + 64 * h + 32, u1);
+        tmem_wait_ld();
+        reg_fence(g0);
+        reg_fence(g1);
+        reg_fence(u0);
+        reg_fence(u1);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty0_lead + 8u * buf);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const uint32_t* g = c ? g1 : g0;
+          const uint32_t* u = c ? u1 : u0;
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+          const uint32_t stg = sStg + (ew * 2 + sbuf) * C::kStgBytes;
+          const uint32_t row_addr = stg + lane * 64;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int i0 = 8 * j + 2 * e;
+              w[e] = pack_bf16x2(silu_mul(__uint_as_float(g[i0]), __uint_as_float(u[i0])),
+                                 silu_mul(__uint_as_float(g[i0 + 1]), __uint_as_float(u[i0 + 1])));
+            }
+            st_shared_v4(row_addr + ((j ^ ((lane >> 1) & 3)) << 4), w[0], w[1], w[2], w[3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int ncol = col0 + 64 * h + 32 * c;
+            if (ncol < p.N && row0 < p.M) tma_store_2d(&p.tmap_y, stg, ncol, row0);
+            bulk_commit();
+          }
+          sbuf ^= 1;
+        }
+      } else if constexpr (kDown) {
         // 256 output columns: accumulator + residual, 32 columns per store
         const __nv_bfloat16* res = reinterpret_cast<const __nv_bfloat16*>(p.residual);
         const int row = row0 + lane;
@@ -387,8 +439,8 @@ cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribut
                                bool with_pdl, bool mx = false) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = mx ? PairCfg::kSmemMx : PairCfg::kSmem;
+  cfg.blockDim = dim3(mx ? PairCfg<true>::kThreadsT : PairCfg<false>::kThreadsT);
+  cfg.dynamicSmemBytes = mx ? PairCfg<true>::kSmem : PairCfg<false>::kSmem;
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -406,19 +458,19 @@ cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribut
 cudaError_t configure_large_m_pair(int* max_pairs) {
   cudaError_t e = cudaFuncSetAttribute(fused_large_m_pair_kernel<false, false, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(PairCfg::kSmem));
+                                       static_cast<int>(PairCfg<false>::kSmem));
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(fused_large_m_pair_kernel<true, false, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(PairCfg::kSmem));
+                             static_cast<int>(PairCfg<false>::kSmem));
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(fused_large_m_pair_kernel<false, true, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(PairCfg::kSmem));
+                             static_cast<int>(PairCfg<false>::kSmem));
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(fused_large_m_pair_kernel<true, false, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(PairCfg::kSmemMx));
+                             static_cast<int>(PairCfg<true>::kSmem));
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pair_config(2, nullptr, attr, false);
@@ -429,11 +481,11 @@ cudaError_t configure_large_m_pair(int* max_pairs) {
   return cudaSuccess;
 }
 
-size_t large_m_pair_smem_bytes() { return PairCfg::kSmem; }
-int large_m_pair_stages() { return PairCfg::kStages; }
+size_t large_m_pair_smem_bytes() { return PairCfg<false>::kSmem; }
+int large_m_pair_stages(bool mx) { return mx ? PairCfg<true>::kStages : PairCfg<false>::kStages; }
 
 cudaError_t launch_large_m_pair(const LargeMParams& p, cudaStream_t stream) {
-  if (p.grid < 2 || (p.grid % 2) != 0 || p.bn != PairCfg::kBN) return cudaErrorInvalidValue;
+  if (p.grid < 2 || (p.grid % 2) != 0 || p.bn != PairCfg<false>::kBN) return cudaErrorInvalidValue;
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pair_config(p.grid, stream, attr, pdl_enabled(), p.mx != 0);
   if (p.fp8 && p.down) return cudaErrorInvalidValue;  // no FP8 down-projection

@@ -84,7 +84,7 @@ cudaError_t launch_large_m(const LargeMParams& p, cudaStream_t stream);
 // also reports how many pairs can be resident at once.
 cudaError_t configure_large_m_pair(int* max_pairs);
 size_t large_m_pair_smem_bytes();
-int large_m_pair_stages();
+int large_m_pair_stages(bool mx = false);
 cudaError_t launch_large_m_pair(const LargeMParams& p, cudaStream_t stream);
 
 // K split over the two CTAs of a cluster, one 128 x 64 output tile per cluster

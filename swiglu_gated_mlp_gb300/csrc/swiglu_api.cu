@@ -632,7 +632,9 @@ swiglu_status_t make_mx_plan(int64_t M, int64_t K, int64_t N, const DeviceState&
   const int64_t kslices = k_slices8(K);
   if (M > 128 || !fp8_uses_decode(M, N, d)) {
     if (d.max_pairs < 1) return SWIGLU_ERR_UNSUPPORTED;
-    return make_plan(M, K, N, SWIGLU_VARIANT_LARGE_M_PAIR, &d, pl, 1);
+    const swiglu_status_t st = make_plan(M, K, N, SWIGLU_VARIANT_LARGE_M_PAIR, &d, pl, 1);
+    pl->stages = swg::large_m_pair_stages(true);
+    return st;
   }
   *pl = Plan{};
   pl->variant = SWIGLU_VARIANT_SMALL_M;
