@@ -26,7 +26,8 @@
 //    of the CTA's first tile (about 64 MB over the grid) and a share of its A
 //    rows, so the first DRAM reads start under the previous grid's tail. On
 //    short loops (the 0.5B shape: 14 slices, 8 stages) staging measured
-//    slower, so it is off there.
+//    slower, both before the wait and right after the first ring-full, so it
+//    is off there.
 #include "kernels.h"
 #include "ptx.cuh"
 

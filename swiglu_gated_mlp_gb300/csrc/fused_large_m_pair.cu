@@ -37,8 +37,8 @@
 // block-scaled form runs 8 epilogue warps (two per tensor-memory lane
 // quarter, 64 output columns each) that load their whole share of the
 // accumulator into registers, release it at once, and only then apply
-// SiLU(g) * u and store; its ring is 5 stages deep to make room for their
-// store staging.
+// SiLU(g) * u and store, each through one store-staging buffer of its own
+// (the wait on its previous store overlaps the next tile's MMAs).
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -51,13 +51,13 @@ struct PairCfg {
   static constexpr int kABytes = 128 * kBlockK * 2;      // 16 KB: this CTA's 128 A rows
   static constexpr int kBBytes = 128 * kBlockK * 2;      // 16 KB: this CTA's 128 weight rows
   static constexpr int kStageBytes = kABytes + kBBytes;  // 32 KB per CTA, 64 KB per pair
-  static constexpr int kStages = kMx ? 5 : 6;
+  static constexpr int kStages = 6;
   static constexpr int kEpiWarps = kMx ? 8 : 4;          // 2 per lane quarter when block-scaled
   static constexpr int kThreadsT = 64 + 32 * kEpiWarps;  // + TMA producer and MMA issuer warps
   static constexpr int kAccCols = 2 * kBN;               // 256 fp32 columns: gate | up
   static constexpr int kTmemCols = 2 * kAccCols;         // double buffered (bf16, per-tensor FP8)
   static constexpr int kStgBytes = 32 * 32 * 2;          // 32 rows x 64 B store staging
-  static constexpr int kNumStg = 2 * kEpiWarps;
+  static constexpr int kNumStg = 8;                      // 2 per warp, or 1 per warp with 8 warps
   static constexpr int kBarBytes = 256;
   // block-scaled FP8: 1.5 KB of scales per stage (A block, gate and up weight blocks)
   static constexpr size_t kSmem = 1024 + size_t(kStages) * kStageBytes +
@@ -298,9 +298,9 @@ __global__ void __launch_bounds__(PairCfg<kMx>::kThreadsT, 1)
         for (int c = 0; c < 2; ++c) {
           const uint32_t* g = c ? g1 : g0;
           const uint32_t* u = c ? u1 : u0;
-          if (lane == 0) bulk_wait_read<1>();
+          if (lane == 0) bulk_wait_read<0>();  // this warp's one staging buffer is free again
           __syncwarp();
-          const uint32_t stg = sStg + (ew * 2 + sbuf) * C::kStgBytes;
+          const uint32_t stg = sStg + ew * C::kStgBytes;
           const uint32_t row_addr = stg + lane * 64;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -320,7 +320,6 @@ __global__ void __launch_bounds__(PairCfg<kMx>::kThreadsT, 1)
             if (ncol < p.N && row0 < p.M) tma_store_2d(&p.tmap_y, stg, ncol, row0);
             bulk_commit();
           }
-          sbuf ^= 1;
         }
       } else if constexpr (kDown) {
         // 256 output columns: accumulator + residual, 32 columns per store
