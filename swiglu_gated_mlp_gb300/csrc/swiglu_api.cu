@@ -626,8 +626,9 @@ size_t mx_weight_scale_bytes(int64_t K, int64_t N) {
 
 // The block-scaled forward's kernel and launch shape: the decode kernel by the
 // FP8 rule, with all tokens in one group (a scale block holds 128 rows from
-// token 0, so M <= 128), the ring sized with the scales, and K split over
-// clusters on narrow N as for the other forms; CTA pairs otherwise.
+// token 0, so M <= 128), the ring sized with the scales, two CTAs per SM when
+// the column blocks outnumber the SMs, and K split over clusters on narrow N
+// as for the other forms; CTA pairs otherwise.
 swiglu_status_t make_mx_plan(int64_t M, int64_t K, int64_t N, const DeviceState& d, Plan* pl) {
   const int64_t kslices = k_slices8(K);
   if (M > 128 || !fp8_uses_decode(M, N, d)) {
@@ -642,6 +643,12 @@ swiglu_status_t make_mx_plan(int64_t M, int64_t K, int64_t N, const DeviceState&
   pl->mt = static_cast<int>((M + 15) / 16 * 16);
   pl->mgroups = 1;
   pl->stages = swg::small_m_stages(pl->mt, 1, swg::kSfStageBytes);
+  if (pl->tiles > d.sm_count) {
+    // more column blocks than SMs: two CTAs per SM keep the whole grid
+    // resident (3+ stages each; accumulators and scale slots in 256 columns)
+    const int s2 = swg::small_m_stages(pl->mt, 2, swg::kSfStageBytes);
+    if (s2 >= 3 && 2 * pl->mt + swg::kSfTmemCols * s2 <= 256) pl->stages = s2;
+  }
   pl->splits = 1;
   const int64_t stage_bytes = 2 * swg::kPackBlockN * swg::kBlockK * 2 + int64_t(pl->mt) * 128;
   if (int64_t(pl->mt) * 1024 <= pl->stages * stage_bytes) {

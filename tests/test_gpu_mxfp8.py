@@ -98,7 +98,8 @@ def test_mx_act_scale_tiles_are_bit_exact(native, M, K):
 # kernel; K multiples of 32 with ragged 128-value slices, ragged N
 CASES = [
     (1, 128, 128), (16, 3584, 1280), (16, 160, 136), (33, 416, 264), (64, 896, 4864),
-    (16, 896, 4864), (48, 512, 20480), (100, 416, 264), (128, 1024, 1024), (200, 512, 1000),
+    (16, 896, 4864), (48, 512, 20480), (1, 512, 27648), (100, 416, 264), (128, 1024, 1024),
+    (200, 512, 1000),
     (300, 512, 1000), (1000, 2048, 768),
 ]
 
@@ -117,6 +118,8 @@ def test_mx_forward_with_scales_random_per_group(native, M, K, N):
 
 def test_mx_plan_string_names_the_kernel(native):
     assert native.swiglu_plan_string_mxfp8(16, 3584, 18944).startswith("mxfp8 small_m")
+    # 216 column blocks for 152 SMs: two decode CTAs per SM (3 stages each)
+    assert "stages=3 " in native.swiglu_plan_string_mxfp8(1, 5120, 27648)
     assert native.swiglu_plan_string_mxfp8(4096, 3584, 18944).startswith("mxfp8 large_m_pair")
     assert "splits=1 " not in native.swiglu_plan_string_mxfp8(16, 896, 4864)
 
