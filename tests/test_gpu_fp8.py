@@ -63,6 +63,11 @@ def test_fp8_forward_matches_oracle(native, M, K, N):
     run_fp8(native, M, K, N, seed=M + 3 * K + N)
 
 
+@pytest.mark.parametrize("M", [1, 2, 3, 7, 15, 16, 17, 127, 128, 129])
+def test_fp8_small_token_counts_match_oracle(native, M):
+    run_fp8(native, M, 400, 264, seed=3000 + M)
+
+
 @pytest.mark.parametrize("name", ["qwen2.5-7b-decode-m16", "qwen2.5-7b-prefill-m4096",
                                   "qwen2.5-72b-prefill-m8192"])
 def test_fp8_full_size_workloads(native, name):

@@ -109,6 +109,11 @@ def test_mx_forward_matches_oracle(native, M, K, N):
     run_mx(native, M, K, N, seed=M + 5 * K + N)
 
 
+@pytest.mark.parametrize("M", [1, 2, 3, 7, 15, 16, 17, 127, 128, 129])
+def test_mx_small_token_counts_match_oracle(native, M):
+    run_mx(native, M, 416, 264, seed=2000 + M)
+
+
 @pytest.mark.parametrize("M,K,N", [(16, 1024, 1280), (33, 416, 264), (64, 896, 4864),
                                    (16, 896, 4864), (300, 512, 1000), (512, 1024, 2048),
                                    (1000, 2048, 768)])

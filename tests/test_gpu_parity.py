@@ -143,6 +143,18 @@ def test_variants_agree(native, variant):
     assert torch.allclose(y_auto.float(), y_var.float(), rtol=1e-2, atol=1e-3)
 
 
+# Every token count from 1 to 17 and around one 128-row tile, on every kernel
+# (ragged K slice and ragged column block): the decode kernel's token padding
+# to 16, the row tails of the 128- and 256-row tiles.
+TOKEN_COUNTS = list(range(1, 18)) + [127, 128, 129]
+
+
+@pytest.mark.parametrize("variant", [AUTO, SMALL, LARGE, PAIR, SPLIT])
+@pytest.mark.parametrize("M", TOKEN_COUNTS)
+def test_every_small_token_count_matches_oracle(native, M, variant):
+    check_against_oracle(native, M, 200, 264, seed=1000 + M, variant=variant)
+
+
 # ------------------------------------------------------------ extremes ----
 
 # Long K (hundreds of pipeline phases per tile), wide N with short K (many
