@@ -278,6 +278,7 @@ cudaError_t configure_split_k(int* max_clusters) {
 }
 
 int split_k_bn() { return SplitCfg::kBN; }
+int split_k_stages() { return SplitCfg::kStages; }
 
 cudaError_t launch_split_k(const LargeMParams& p, cudaStream_t stream) {
   if (p.bn != SplitCfg::kBN || p.grid != 2 * p.tiles_m * p.tiles_n || p.fp8 || p.down || p.mx)

@@ -92,6 +92,7 @@ cudaError_t launch_large_m_pair(const LargeMParams& p, cudaStream_t stream);
 // than one SM's shared memory holds.
 cudaError_t configure_split_k(int* max_clusters);
 int split_k_bn();
+int split_k_stages();
 cudaError_t launch_split_k(const LargeMParams& p, cudaStream_t stream);
 
 // Sequential gate-then-up schedule (bn = 128, 128-row tiles), an ablation.

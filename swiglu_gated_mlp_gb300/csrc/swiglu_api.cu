@@ -383,7 +383,7 @@ swiglu_status_t make_plan(int64_t M, int64_t K, int64_t N, int variant, const De
     if (split_clusters < 1 || elem_bytes != 2) return SWIGLU_ERR_UNSUPPORTED;
     if (split_tiles > 1073741823) return SWIGLU_ERR_UNSUPPORTED;
     pl->bn = static_cast<int>(split_bn);
-    pl->stages = 7;
+    pl->stages = swg::split_k_stages();
     pl->tiles_m = static_cast<int>((M + swg::kTileM - 1) / swg::kTileM);
     pl->tiles_n = static_cast<int>((N + split_bn - 1) / split_bn);
     pl->group_m = 1;
