@@ -28,12 +28,17 @@
 //
 // With kMx (block-scaled E4M3: one power-of-two scale per 32 K values) each
 // CTA also loads, per stage, the scale block of its 128 A rows and both of the
-// packed tile's weight-scale blocks (gate, up: the MMA's 256 B columns); the
-// even CTA copies them into a per-stage slot of both CTAs' tensor memory
-// (tcgen05.cp.cta_group::2, each CTA from its own shared memory) and issues
-// kind::mxf8f6f4 MMAs. The scale slots take the second half of tensor memory,
-// so the accumulator is single-buffered: the next tile's MMAs wait for the
-// epilogue to have read the previous one. To keep that wait short the
+// packed tile's weight-scale blocks (gate, up: the MMA's 256 B columns). A
+// warp of the even CTA of its own copies them, as soon as a stage has landed,
+// into that stage's slot of both CTAs' tensor memory (tcgen05.cp.cta_group::2,
+// each CTA from its own shared memory) and signals their completion on a
+// per-stage barrier; the MMA issuer waits for it and issues kind::mxf8f6f4
+// MMAs, so the copies never sit in the MMA issuer's own stream of tensor
+// instructions (copies issued there, just before the MMAs that read them,
+// left the tensor pipe idle for a while at every stage; issuing them one stage
+// early there was slower still). The scale slots take the second half of
+// tensor memory, so the accumulator is single-buffered: the next tile's MMAs
+// wait for the epilogue to have read the previous one. To keep that wait short the
 // block-scaled form runs 8 epilogue warps (two per tensor-memory lane
 // quarter, 64 output columns each) that load their whole share of the
 // accumulator into registers, release it at once, and only then apply
@@ -53,7 +58,9 @@ struct PairCfg {
   static constexpr int kStageBytes = kABytes + kBBytes;  // 32 KB per CTA, 64 KB per pair
   static constexpr int kStages = 6;
   static constexpr int kEpiWarps = kMx ? 8 : 4;          // 2 per lane quarter when block-scaled
-  static constexpr int kThreadsT = 64 + 32 * kEpiWarps;  // + TMA producer and MMA issuer warps
+  // TMA producer and MMA issuer warps, the epilogue warps, and (block-scaled)
+  // a warp that copies each stage's scales into tensor memory
+  static constexpr int kThreadsT = 64 + 32 * kEpiWarps + (kMx ? 32 : 0);
   static constexpr int kAccCols = 2 * kBN;               // 256 fp32 columns: gate | up
   static constexpr int kTmemCols = 2 * kAccCols;         // double buffered (bf16, per-tensor FP8)
   static constexpr int kStgBytes = 32 * 32 * 2;          // 32 rows x 64 B store staging
@@ -64,6 +71,7 @@ struct PairCfg {
                                   size_t(kNumStg) * kStgBytes +
                                   (kMx ? size_t(kStages) * kSfStageBytes : 0) + kBarBytes;
   static_assert(kSmem <= 232448, "shared memory budget");
+  static_assert(8 * (3 * kStages + 6) + 8 <= kBarBytes, "barrier slots");
   static constexpr int kSfCol = kAccCols;  // scale slots after the single accumulator
   static_assert(!kMx || kSfCol + kStages * kSfTmemCols <= kTmemCols, "tensor memory budget");
 };
@@ -97,11 +105,13 @@ __global__ void __launch_bounds__(PairCfg<kMx>::kThreadsT, 1)
   uint8_t* bar_ptr = smem + size_t(C::kStages) * C::kStageBytes + C::kNumStg * C::kStgBytes +
                      (kMx ? size_t(C::kStages) * kSfStageBytes : 0);
   const uint32_t bar0 = smem_addr(bar_ptr);
-  // barrier slots: full[S] | empty[S] | tmem_full[2] | tmem_empty[2] | drain
+  // barrier slots: full[S] | empty[S] | tmem_full[2] | tmem_empty[2] | drain |
+  // scales_ready[S] | scale-copy drain
   const uint32_t full0 = bar0, empty0 = bar0 + 8u * C::kStages;
   const uint32_t tfull0 = bar0 + 16u * C::kStages, tempty0 = tfull0 + 16u;
   const uint32_t drain_bar = tempty0 + 16u;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_ptr + 8 * (2 * C::kStages + 5));
+  const uint32_t sready0 = drain_bar + 8u, sdrain_bar = sready0 + 8u * C::kStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_ptr + 8 * (3 * C::kStages + 6));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -134,6 +144,8 @@ __global__ void __launch_bounds__(PairCfg<kMx>::kThreadsT, 1)
       mbar_init(tempty0 + 8u * b, 2 * C::kEpiWarps);  // epilogue warps x 2 CTAs (used on rank 0)
     }
     mbar_init(drain_bar, 1);
+    for (int s = 0; s < C::kStages; ++s) mbar_init(sready0 + 8u * s, 1);  // scale-copy commit
+    mbar_init(sdrain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -218,17 +230,17 @@ __global__ void __launch_bounds__(PairCfg<kMx>::kThreadsT, 1)
             ok = false;
             break;
           }
+          // block-scaled: the scale-copy warp has put this stage's scales in
+          // its tensor-memory slot
+          if (kMx && !mbar_wait(sready0 + 8u * s, ph, wc, kSiteMmaFull)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint64_t adesc = smem_desc_sw128(sA + s * C::kABytes);
           const uint64_t bdesc = smem_desc_sw128(sB + s * C::kBBytes);
           // scale slot of this stage: A rows [0, 4), B columns 0..127 [4, 8), 128..255 [8, 12)
           const uint32_t tsf = tmem_base + C::kSfCol + uint32_t(s) * kSfTmemCols;
-          if constexpr (kMx) {
-            const uint32_t sf = sSf + s * kSfStageBytes;
-            tmem_cp_sf_pair(tsf, smem_desc_sf(sf));
-            tmem_cp_sf_pair(tsf + 4, smem_desc_sf(sf + kSfBlockBytes));
-            tmem_cp_sf_pair(tsf + 8, smem_desc_sf(sf + 2 * kSfBlockBytes));
-          }
 #pragma unroll
           for (int k = 0; k < 4; ++k) {  // four 32-byte K steps per 128-byte row
             if constexpr (kMx)  // K step k consumes scale group k of the slice (IDs at bits 4, 29)
@@ -255,6 +267,40 @@ __global__ void __launch_bounds__(PairCfg<kMx>::kThreadsT, 1)
       }
       mma_commit_pair_multicast(drain_bar, 0x1);
       mbar_wait_drain(drain_bar, 0, wc);
+    }
+    __syncwarp();
+  } else if (kMx && warp == 2 + C::kEpiWarps) {
+    // ------------------------------------------------ scale copies (rank 0)
+    // Each stage's scales go from shared to tensor memory (both CTAs, each
+    // from its own shared memory) as soon as the stage has landed, in a
+    // stream of tcgen05 operations of their own, and the MMA issuer waits
+    // for their completion. A slot is refilled only after its stage was
+    // refilled, i.e. after the MMAs that read its previous contents completed.
+    if (leader && lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int t = pair; ok && t < num_tiles; t += pairs) {
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(full0 + 8u * s, ph, wc, kSiteScaleCopy)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t tsf = tmem_base + C::kSfCol + uint32_t(s) * kSfTmemCols;
+          const uint32_t sf = sSf + s * kSfStageBytes;
+          tmem_cp_sf_pair(tsf, smem_desc_sf(sf));
+          tmem_cp_sf_pair(tsf + 4, smem_desc_sf(sf + kSfBlockBytes));
+          tmem_cp_sf_pair(tsf + 8, smem_desc_sf(sf + 2 * kSfBlockBytes));
+          mma_commit_pair_multicast(sready0 + 8u * s, 0x1);
+          if (++s == C::kStages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      mma_commit_pair_multicast(sdrain_bar, 0x1);
+      mbar_wait_drain(sdrain_bar, 0, wc);
     }
     __syncwarp();
   } else {

@@ -82,6 +82,7 @@ enum WaitSite : uint32_t {
   kSiteMmaTmemEmpty = 3,
   kSiteEpiTmemFull = 4,
   kSiteDrain = 5,
+  kSiteScaleCopy = 6,
 };
 
 struct WaitCtx {
