@@ -100,7 +100,7 @@ CASES = [
     (1, 128, 128), (16, 3584, 1280), (16, 160, 136), (33, 416, 264), (64, 896, 4864),
     (16, 896, 4864), (48, 512, 20480), (1, 512, 27648), (100, 416, 264), (128, 1024, 1024),
     (200, 512, 1000),
-    (300, 512, 1000), (1000, 2048, 768),
+    (300, 512, 1000), (1000, 2048, 768), (257, 160, 136), (300, 416, 264), (513, 96, 4864),
 ]
 
 
