@@ -313,7 +313,12 @@ def prepare(args, sg, w: Workload, dev) -> Prepared:
         r0 = r_cpu.to(dev)
         Rs = [r0] + [r0.clone() for _ in range(copies - 1)]
     variant = VARIANTS[args.variant]
-    plan = (sg.swiglu_down_plan_string(M, N, K) if down else
+    # down-projection: a workspace lets the decode kernel split K across
+    # clusters; one per stream of calls (the timed graph is one stream)
+    down_ws = down and args.down_workspace == "on"
+    ws = sg.swiglu_down_workspace(M, N, K, dev) if down_ws else None
+    plan = ((sg.swiglu_down_plan_string_ws if down_ws else sg.swiglu_down_plan_string)(M, N, K)
+            if down else
             sg.swiglu_plan_string_mxfp8(M, K, N) if mx else
             sg.swiglu_plan_string_fp8(M, K, N) if fp8 else
             sg.swiglu_plan_string(M, K, N, variant))
@@ -329,7 +334,7 @@ def prepare(args, sg, w: Workload, dev) -> Prepared:
     def fwd(j, s=None):
         """One forward on rotation slot j (on stream s, default the current stream)."""
         if down:
-            sg.swiglu_down_forward(As[j], wps[j], K, R=Rs[j], Out=Ys[j], stream=s)
+            sg.swiglu_down_forward(As[j], wps[j], K, R=Rs[j], Out=Ys[j], stream=s, workspace=ws)
         elif mx:
             sg.swiglu_forward_mxfp8(As[j], SAs[j], wps[j], N, Y=Ys[j], stream=s)
         elif fp8:
@@ -342,7 +347,8 @@ def prepare(args, sg, w: Workload, dev) -> Prepared:
     return Prepared(w=w, fp8=fp8, down=down, flops=flops, alg_bytes=alg_bytes, copies=copies,
                     plan=plan, kernel=kernel, fwd=fwd, out_cols=out_cols, w_bytes=w_bytes,
                     a_cpu=a_cpu, host=host,
-                    dev_state={"wps": wps, "As": As, "Ys": Ys, "Rs": Rs, "SAs": SAs})
+                    dev_state={"wps": wps, "As": As, "Ys": Ys, "Rs": Rs, "SAs": SAs,
+                               "down_ws": down_ws})
 
 
 def time_steps(args, sg, pr: Prepared, steps: int, world: int, dev, stream):
@@ -476,6 +482,9 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     e2e_streams = [stream, torch.cuda.Stream(device=dev)]
     a_dev = [torch.empty(*a_cpu.shape, dtype=a_cpu.dtype, device=dev) for _ in e2e_streams]
     y_dev = [torch.empty(M, out_cols, dtype=torch.bfloat16, device=dev) for _ in e2e_streams]
+    # down-projection with a workspace: one per stream, as the streams overlap
+    e2e_ws = [sg.swiglu_down_workspace(M, N, K, dev) if pr.dev_state.get("down_ws") else None
+              for _ in e2e_streams]
     mx = "sat" in pr.host
     if mx:  # A's block scales travel with A every step
         sa_host = [pr.host["sat"].pin_memory() for _ in a_host]
@@ -490,7 +499,7 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
             with torch.cuda.stream(st):
                 a_dev[b].copy_(a_host[j], non_blocking=True)
                 sg.swiglu_down_forward(a_dev[b], wps[i % copies], K, R=Rs[i % copies],
-                                       Out=y_dev[b], stream=st)
+                                       Out=y_dev[b], stream=st, workspace=e2e_ws[b])
                 y_host[j].copy_(y_dev[b], non_blocking=True)
         elif mx:  # host copies through torch around the block-scaled call
             with torch.cuda.stream(st):
@@ -884,6 +893,8 @@ def main(argv=None):
                    help="rotating copies of the operands (0: enough that 32 x L2 bytes of "
                         "other copies are read between two uses of one)")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--down-workspace", choices=["on", "off"], default="on",
+                   help="--op down: pass a workspace (K split across clusters allowed) or not")
     p.add_argument("--op", choices=["swiglu", "down"], default="swiglu",
                    help="swiglu: the fused gate/up projection (default); down: Out = Y W3 + R")
     p.add_argument("--dtype", choices=["bf16", "fp8", "mxfp8"], default="bf16",

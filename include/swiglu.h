@@ -310,6 +310,41 @@ SWIGLU_API swiglu_status_t swiglu_down_plan_string(int64_t M, int64_t N, int64_t
                                                    size_t buflen);
 
 /*
+ * Down-projection with a caller workspace. With few 256-column output blocks
+ * and few tokens (the decode kernel), one cluster of CTAs per block leaves
+ * most SMs idle while the weight stream is the whole cost; with a workspace
+ * the block's K range is also split across several clusters, which write fp32
+ * partial sums to the workspace, and the last cluster of each block to finish
+ * adds them in cluster order (so results do not depend on timing) and writes
+ * Out. Same result rule as swiglu_down_forward; the two may differ in the
+ * last bits of the fp32 sums (a different summation order) before rounding.
+ *
+ * swiglu_down_workspace_bytes(M, N, H): bytes that call needs for (M, N, H) on
+ *   the current device; 0 when its plan does not split K across clusters (or
+ *   on a bad shape or no usable device).
+ * swiglu_down_forward_ws: as swiglu_down_forward, plus `workspace` (device,
+ *   16-byte aligned, overlapping no other argument) of `workspace_bytes`.
+ *   workspace NULL: exactly swiglu_down_forward. Otherwise, if the plan needs
+ *   a workspace, workspace_bytes below swiglu_down_workspace_bytes or a bad
+ *   pointer: INVALID_ARG. Contents: the first bytes hold arrival counters that
+ *   must be zero when a call's kernel starts; the caller zero-fills the
+ *   workspace once before its first use, and every call's kernel leaves them
+ *   at zero again when it ends (also when a pipeline wait timed out), so a
+ *   workspace serves any number of calls in stream order. Calls that may run
+ *   at the same time (different streams) need separate workspaces. The
+ *   library never allocates it.
+ * swiglu_down_plan_string_ws: the plan swiglu_down_forward_ws takes with a
+ *   workspace ("clusters=g": K split across g clusters per block).
+ */
+SWIGLU_API size_t swiglu_down_workspace_bytes(int64_t M, int64_t N, int64_t H);
+SWIGLU_API swiglu_status_t swiglu_down_forward_ws(const void* Y, const void* W3packed,
+                                                  const void* R, void* Out, int64_t M, int64_t N,
+                                                  int64_t H, void* workspace,
+                                                  size_t workspace_bytes, swiglu_stream_t stream);
+SWIGLU_API swiglu_status_t swiglu_down_plan_string_ws(int64_t M, int64_t N, int64_t H, char* buf,
+                                                      size_t buflen);
+
+/*
  * Allocation-free forward for callers that cannot call cudaMalloc: serving
  * runtimes that reserve all device memory for their own pools up front (a
  * library allocation would fail, or would fragment memory the runtime plans

@@ -19,6 +19,7 @@ _EXPORTS = {
     "swiglu_forward_noalloc", "swiglu_pack_weights_fp8", "swiglu_forward_fp8",
     "swiglu_packed_weight_bytes_fp8", "swiglu_down_packed_bytes", "swiglu_pack_down_weights",
     "swiglu_down_forward", "swiglu_down_plan_string", "swiglu_plan_string_fp8",
+    "swiglu_down_workspace_bytes", "swiglu_down_workspace", "swiglu_down_plan_string_ws",
     "swiglu_packed_weight_bytes", "swiglu_check_device_status", "swiglu_status_string",
     "swiglu_plan_string", "swiglu_testing_inject_stall", "SwigluError",
     "SWIGLU_VARIANT_AUTO", "SWIGLU_VARIANT_LARGE_M", "SWIGLU_VARIANT_SMALL_M",

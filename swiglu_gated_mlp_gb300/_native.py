@@ -68,6 +68,12 @@ lib.swiglu_down_forward.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]
 lib.swiglu_down_forward.restype = _int
 lib.swiglu_down_plan_string.argtypes = [_i64, _i64, _i64, ctypes.c_char_p, _sz]
 lib.swiglu_down_plan_string.restype = _int
+lib.swiglu_down_workspace_bytes.argtypes = [_i64, _i64, _i64]
+lib.swiglu_down_workspace_bytes.restype = _sz
+lib.swiglu_down_forward_ws.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _vp]
+lib.swiglu_down_forward_ws.restype = _int
+lib.swiglu_down_plan_string_ws.argtypes = [_i64, _i64, _i64, ctypes.c_char_p, _sz]
+lib.swiglu_down_plan_string_ws.restype = _int
 lib.swiglu_plan_string_fp8.argtypes = [_i64, _i64, _i64, ctypes.c_char_p, _sz]
 lib.swiglu_plan_string_fp8.restype = _int
 lib.swiglu_packed_weight_bytes_mxfp8.argtypes = [_i64, _i64]
@@ -392,10 +398,41 @@ def swiglu_down_plan_string(M: int, N: int, H: int) -> str:
     return buf.value.decode()
 
 
+def swiglu_down_plan_string_ws(M: int, N: int, H: int) -> str:
+    buf = ctypes.create_string_buffer(256)
+    _check(lib.swiglu_down_plan_string_ws(int(M), int(N), int(H), buf, 256),
+           "swiglu_down_plan_string_ws")
+    return buf.value.decode()
+
+
+def swiglu_down_workspace_bytes(M: int, N: int, H: int) -> int:
+    return int(lib.swiglu_down_workspace_bytes(int(M), int(N), int(H)))
+
+
+def swiglu_down_workspace(M: int, N: int, H: int, device=None) -> torch.Tensor | None:
+    """A zero-filled workspace for swiglu_down_forward(..., workspace=) at (M, N, H), or None.
+
+    One workspace serves any number of calls in stream order (each call leaves
+    its counters at zero); calls that may overlap in time need one each.
+    """
+    if device is None:
+        device = torch.device("cuda", torch.cuda.current_device())
+    device = torch.device(device)
+    with _on_device(device):
+        n = swiglu_down_workspace_bytes(M, N, H)
+    if n == 0:
+        return None
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
 def swiglu_down_forward(Y: torch.Tensor, W3packed: torch.Tensor, H: int,
                         R: torch.Tensor | None = None, Out: torch.Tensor | None = None,
-                        stream=None) -> torch.Tensor:
-    """Out [M, H] = Y [M, N] x W3 + R (R optional; Out may be R for an in-place add)."""
+                        stream=None, workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Out [M, H] = Y [M, N] x W3 + R (R optional; Out may be R for an in-place add).
+
+    With `workspace` (from swiglu_down_workspace, on Y's device) the decode
+    kernel may also split K across clusters (swiglu_down_forward_ws).
+    """
     _dev_bf16(Y, "Y")
     _dev_bf16(W3packed, "W3packed")
     if Y.dim() != 2:
@@ -412,6 +449,16 @@ def swiglu_down_forward(Y: torch.Tensor, W3packed: torch.Tensor, H: int,
     _dev_bf16(Out, "Out")
     if tuple(Out.shape) != (M, H):
         raise ValueError("Out must be [M, H]")
+    if workspace is not None:
+        if not workspace.is_cuda or workspace.device != Y.device or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor on Y's device")
+        with _on_device(Y.device):
+            _check(lib.swiglu_down_forward_ws(
+                Y.data_ptr(), W3packed.data_ptr(), R.data_ptr() if R is not None else None,
+                Out.data_ptr(), M, N, H, workspace.data_ptr(),
+                workspace.numel() * workspace.element_size(), _stream_handle(stream, Y.device)),
+                "swiglu_down_forward_ws")
+        return Out
     with _on_device(Y.device):
         _check(lib.swiglu_down_forward(Y.data_ptr(), W3packed.data_ptr(),
                                        R.data_ptr() if R is not None else None, Out.data_ptr(),

@@ -20,7 +20,12 @@
 // TMEM, writes the fp32 partial Gate and Up to its own shared memory, and after
 // a cluster barrier each CTA sums, through distributed shared memory, all
 // parts of its share of the block's columns, applies SiLU(g) * u and writes
-// those outputs. No global scratch is used.
+// those outputs. No global scratch is used. With a caller workspace the K
+// range can also be split across `gsplits` such clusters (more CTAs than
+// clusters of 8 can hold): each cluster writes its summed shares to the
+// workspace and counts itself in, and the last cluster of the block to arrive
+// (one counter per cluster rank) adds all clusters' partials in cluster order,
+// so the result does not depend on arrival order, and finishes the outputs.
 //
 // The same kernel computes the gated MLP's down-projection Out = Y x W3 + R
 // (kDown): a packed tile then holds 256 consecutive output columns, the two
@@ -48,6 +53,7 @@ constexpr int kWStageBytes = 2 * kPackBlockN * kBlockK * 2;  // 32 KB: 256 packe
 static __device__ __align__(256) uint32_t g_static_scratch[kStaticScratchWords];
 
 constexpr int kMaxStages = 8;
+constexpr int kMaxClusters = 8;  // K split across at most this many clusters per unit
 constexpr size_t kSmemLimit = 232448;
 constexpr int kBarBytes = 256;
 
@@ -84,15 +90,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int num_kb = (p.K + kBK - 1) / kBK;
   const int splits = p.splits > 1 ? p.splits : 1;
-  // CTA index = ((column block * token groups) + token group) * splits + K part
+  const int gsplits = p.gsplits > 1 ? p.gsplits : 1;
+  // CTA index = ((unit * gsplits) + cluster) * splits + rank in the cluster,
+  // unit = column block * token groups + token group
   const int mgroups = p.mgroups > 1 ? p.mgroups : 1;
   const int part = blockIdx.x % splits;  // the CTA's rank in its cluster when splits > 1
-  const int tgroup = (blockIdx.x / splits) % mgroups;
-  const int nblk = blockIdx.x / (splits * mgroups);
+  const int gpart = (blockIdx.x / splits) % gsplits;
+  const int unit = blockIdx.x / (splits * gsplits);
+  const int tgroup = unit % mgroups;
+  const int nblk = unit / mgroups;
   const int m0 = tgroup * mt;                 // first token of this CTA's group
   const int mcount = min(mt, p.M - m0);       // tokens in the group
-  const int kb_begin = part * num_kb / splits;
-  const int kb_end = (part + 1) * num_kb / splits;
+  const int kparts = splits * gsplits;        // K parts of the unit, in order
+  const int kpart = gpart * splits + part;
+  const int kb_begin = kpart * num_kb / kparts;
+  const int kb_end = (kpart + 1) * num_kb / kparts;
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
 
   if (threadIdx.x == 0) {
@@ -232,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int ok = 1;
     if (lane == 0) ok = mbar_wait(tfull_bar, 0, wc, kSiteEpiTmemFull) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok && splits > 1) {
+    if (ok && kparts > 1) {
       // K part only: fp32 partials to this CTA's shared memory (the ring is idle
       // now), as P[c][r] for accumulator column c (gate 0..mt-1, up mt..2mt-1)
       // and weight row r of the block.
@@ -306,26 +318,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   }
 
-  if (splits > 1) {
-    cluster_sync();  // every part's partials are in its CTA's shared memory
+  if (kparts > 1) {
+    // every part's partials are in its CTA's shared memory
+    if (splits > 1)
+      cluster_sync();
+    else
+      __syncthreads();
     // This CTA finishes weight rows [part * R, part * R + R) of the block for
     // all tokens: sum the parts (fixed order), SiLU(g) * u, 4 columns per item.
     const int rows = kPackBlockN / splits;
     const int chunks = rows / 4;
     const uint32_t local = smem_addr(smem);
     __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(p.y);
-    for (int idx = threadIdx.x; idx < mcount * chunks; idx += blockDim.x) {
-      const int m = idx / chunks;
-      const int r = part * rows + (idx % chunks) * 4;
-      float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
-      for (int s = 0; s < splits; ++s) {
-        const uint32_t base = mapa_shared(local, static_cast<uint32_t>(s));
-        const float4 gs = ld_shared_cluster_v4(base + 4u * static_cast<uint32_t>(m * kPackBlockN + r));
-        const float4 us =
-            ld_shared_cluster_v4(base + 4u * static_cast<uint32_t>((mt + m) * kPackBlockN + r));
-        g.x += gs.x; g.y += gs.y; g.z += gs.z; g.w += gs.w;
-        u.x += us.x; u.y += us.y; u.z += us.z; u.w += us.w;
-      }
+    // the outputs of token m, weight rows r .. r + 3 of the block, from the summed g and u
+    auto finish = [&](int m, int r, float4 g, float4 u) {
       if constexpr (kDown) {  // columns n0 + r .. + 3 (g) and n0 + 128 + r .. + 3 (u)
         const __nv_bfloat16* res = reinterpret_cast<const __nv_bfloat16*>(p.residual);
         const int n_lo = nblk * 2 * kPackBlockN + r, n_hi = n_lo + kPackBlockN;
@@ -348,21 +354,105 @@ __global__ void __launch_bounds__(kThreads, 1)
           o.y = pack_bf16x2(v.z, v.w);
           *reinterpret_cast<uint2*>(y + row + cols[h]) = o;
         }
-        continue;
+      } else {
+        const int n = nblk * kPackBlockN + r;  // N % 8 == 0: n < N implies n + 3 < N
+        if (kFp8) {
+          g.x *= p.scale_gate; g.y *= p.scale_gate; g.z *= p.scale_gate; g.w *= p.scale_gate;
+          u.x *= p.scale_up; u.y *= p.scale_up; u.z *= p.scale_up; u.w *= p.scale_up;
+        }
+        if (n < p.N) {
+          uint2 v;
+          v.x = pack_bf16x2(silu_mul(g.x, u.x), silu_mul(g.y, u.y));
+          v.y = pack_bf16x2(silu_mul(g.z, u.z), silu_mul(g.w, u.w));
+          *reinterpret_cast<uint2*>(y + static_cast<size_t>(m0 + m) * p.N + n) = v;
+        }
       }
-      const int n = nblk * kPackBlockN + r;  // N % 8 == 0: n < N implies n + 3 < N
-      if (kFp8) {
-        g.x *= p.scale_gate; g.y *= p.scale_gate; g.z *= p.scale_gate; g.w *= p.scale_gate;
-        u.x *= p.scale_up; u.y *= p.scale_up; u.z *= p.scale_up; u.w *= p.scale_up;
+    };
+    // K split across clusters: this cluster's sums, [g rows | u rows] x mt x 128
+    // floats per (unit, cluster)
+    const size_t ws_stride = size_t(2) * mt * kPackBlockN;
+    for (int idx = threadIdx.x; idx < mcount * chunks; idx += blockDim.x) {
+      const int m = idx / chunks;
+      const int r = part * rows + (idx % chunks) * 4;
+      float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+#pragma unroll 2
+      for (int s = 0; s < splits; ++s) {
+        float4 gs, us;
+        if (splits > 1) {
+          const uint32_t base = mapa_shared(local, static_cast<uint32_t>(s));
+          gs = ld_shared_cluster_v4(base + 4u * static_cast<uint32_t>(m * kPackBlockN + r));
+          us = ld_shared_cluster_v4(base + 4u * static_cast<uint32_t>((mt + m) * kPackBlockN + r));
+        } else {
+          const float* own = reinterpret_cast<const float*>(smem);
+          gs = *reinterpret_cast<const float4*>(own + m * kPackBlockN + r);
+          us = *reinterpret_cast<const float4*>(own + (mt + m) * kPackBlockN + r);
+        }
+        g.x += gs.x; g.y += gs.y; g.z += gs.z; g.w += gs.w;
+        u.x += us.x; u.y += us.y; u.z += us.z; u.w += us.w;
       }
-      if (n < p.N) {
-        uint2 v;
-        v.x = pack_bf16x2(silu_mul(g.x, u.x), silu_mul(g.y, u.y));
-        v.y = pack_bf16x2(silu_mul(g.z, u.z), silu_mul(g.w, u.w));
-        *reinterpret_cast<uint2*>(y + static_cast<size_t>(m0 + m) * p.N + n) = v;
+      if (gsplits > 1) {
+        float* mine = p.ws + (size_t(unit) * gsplits + gpart) * ws_stride;
+        *reinterpret_cast<float4*>(mine + size_t(m) * kPackBlockN + r) = g;
+        *reinterpret_cast<float4*>(mine + size_t(mt + m) * kPackBlockN + r) = u;
+      } else {
+        finish(m, r, g, u);
       }
     }
-    cluster_sync();  // no CTA leaves while a peer may still read its partials
+    if (splits > 1) cluster_sync();  // no CTA leaves while a peer may still read its partials
+    if (gsplits > 1) {
+      // Every CTA of every cluster counts itself in exactly once, whatever its
+      // waits returned, so the counter is back at zero when the kernel ends.
+      volatile int* last_flag = abort_flag + 1;
+      __syncthreads();  // all of this CTA's partial stores are issued
+      if (threadIdx.x == 0) {
+        __threadfence();  // (cumulative) they are visible before this CTA is counted
+        uint32_t* counter = p.counters + size_t(unit) * splits + part;
+        const uint32_t before = atomicAdd(counter, 1u);
+        const bool last = before == static_cast<uint32_t>(gsplits - 1);
+        if (last) {
+          atomicExch(counter, 0u);  // every cluster of the unit has arrived
+          __threadfence();          // and their partials are visible to this CTA
+        }
+        *last_flag = last ? 1 : 0;
+      }
+      __syncthreads();
+      if (*last_flag) {
+        // kSumBatch outputs per thread at a time, the loads of all clusters
+        // issued before the sums (in cluster order: independent of arrival order)
+        constexpr int kSumBatch = 4;
+        const int items = mcount * chunks;
+        for (int i0 = threadIdx.x; i0 < items; i0 += kSumBatch * blockDim.x) {
+          float4 g[kSumBatch], u[kSumBatch];
+#pragma unroll
+          for (int b = 0; b < kSumBatch; ++b) g[b] = u[b] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int c = 0; c < kMaxClusters; ++c) {
+            if (c < gsplits) {
+              const float* src = p.ws + (size_t(unit) * gsplits + c) * ws_stride;
+              float4 gs[kSumBatch], us[kSumBatch];
+#pragma unroll
+              for (int b = 0; b < kSumBatch; ++b) {
+                const int idx = min(i0 + b * static_cast<int>(blockDim.x), items - 1);
+                const int m = idx / chunks;
+                const int r = part * rows + (idx % chunks) * 4;
+                gs[b] = __ldcg(reinterpret_cast<const float4*>(src + size_t(m) * kPackBlockN + r));
+                us[b] = __ldcg(reinterpret_cast<const float4*>(src + size_t(mt + m) * kPackBlockN + r));
+              }
+#pragma unroll
+              for (int b = 0; b < kSumBatch; ++b) {
+                g[b].x += gs[b].x; g[b].y += gs[b].y; g[b].z += gs[b].z; g[b].w += gs[b].w;
+                u[b].x += us[b].x; u[b].y += us[b].y; u[b].z += us[b].z; u[b].w += us[b].w;
+              }
+            }
+          }
+#pragma unroll
+          for (int b = 0; b < kSumBatch; ++b) {
+            const int idx = i0 + b * static_cast<int>(blockDim.x);
+            if (idx < items) finish(idx / chunks, part * rows + (idx % chunks) * 4, g[b], u[b]);
+          }
+        }
+      }
+    }
   }
 
   tc_fence_before();
@@ -443,12 +533,16 @@ cudaError_t launch_small_m(const SmallMParams& p, cudaStream_t stream) {
   if (p.stages < 2 || p.stages > kMaxStages || p.mt < 16 || p.mt > 256 || (p.mt % 16) != 0)
     return cudaErrorInvalidValue;
   const int splits = p.splits > 1 ? p.splits : 1;
+  const int gsplits = p.gsplits > 1 ? p.gsplits : 1;
   const int bk = p.fp8 ? kBlockK8 : kBlockK;
   const int num_kb = (p.K + bk - 1) / bk;
-  if (splits > 1 &&
-      (splits > 8 || (kPackBlockN % (4 * splits)) != 0 || splits > num_kb || p.mt > 128 ||
+  if (splits * gsplits > 1 &&
+      (splits > 8 || (kPackBlockN % (4 * splits)) != 0 || splits * gsplits > num_kb || p.mt > 128 ||
        size_t(2) * p.mt * kPackBlockN * 4 > size_t(p.stages) * (kWStageBytes + size_t(p.mt) * kBlockK * 2) ||
-       (p.grid % splits) != 0))
+       (p.grid % (splits * gsplits)) != 0))
+    return cudaErrorInvalidValue;
+  if (gsplits > 1 && (gsplits > kMaxClusters || !p.ws || !p.counters ||
+                      (reinterpret_cast<uintptr_t>(p.ws) & 15u) != 0))
     return cudaErrorInvalidValue;
   // block-scaled FP8: one 128-token group (the scale blocks cover 128 rows
   // from m0 = 0) and 2 mt accumulator columns + the scale slots within 512

@@ -51,7 +51,7 @@ struct SmallMParams {
   int M, K, N;
   int mt;      // tokens rounded up to a multiple of 16 (MMA N), <= 256
   int stages;  // pipeline depth
-  int grid;    // one CTA per 128-column block and K part (splits)
+  int grid;    // one CTA per 128-column block, token group and K part (splits x gsplits)
   int splits;  // K parts per column block (<= 1: none); > 1: clusters of `splits` CTAs
   int mgroups; // token groups of mt rows each (<= 1: one group holds all M tokens)
   int fp8;     // E4M3 inputs: accumulators are scaled by scale_gate / scale_up
@@ -66,6 +66,13 @@ struct SmallMParams {
   uint64_t timeout_ns;
   int inject_stall;
   int l2_prefetch;  // packed tiles per CTA staged in L2 before the grid-dependency wait
+  // K split across clusters (gsplits > 1): each cluster's reduced fp32 partials
+  // go to ws, per (unit, cluster) 2 * mt * 128 floats; counters (one per unit
+  // and cluster rank, zero before the launch and again after it) elect the
+  // last cluster of a unit, which sums all partials in cluster order
+  int gsplits;
+  float* ws;
+  uint32_t* counters;
 };
 
 // One-time per-device set-up (dynamic shared-memory limits of every instantiation).

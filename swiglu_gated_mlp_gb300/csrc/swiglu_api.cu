@@ -309,12 +309,64 @@ void decode_split_plan(int64_t M, int64_t blocks, int64_t kslices, const DeviceS
 struct DownPlan {
   bool decode = false;
   int mt = 0, mgroups = 1, stages = 0, splits = 1, grid = 0;  // splits: decode clusters
+  int gsplits = 1;  // decode: clusters per unit (K split across clusters, caller workspace)
   int64_t blocks = 0, pm = 0, tiles = 0, group = 1;
 };
 
-// The down-projection's kernel and launch shape.
+// Decode-kernel K split across clusters, for a call with a workspace. It adds
+// a tail to every launch (partial sums to the workspace, a fence and a counter,
+// and the last cluster's final sum: about 3 us), so it is taken only where it
+// raises the CTA count by at least 40 % over the plan without it, and with
+// token tiles of at most 32 (the tail grows with the tile). Then the largest
+// cluster size s and, for it, the most clusters g per unit (at most 8) with
+// every CTA resident at once (one per SM; clusters of s must all fit). From a
+// sweep of (s, g) on the 7B, 32B and 72B shapes at M = 1..64 and the 0.5B
+// shape: 32B (20 blocks) at M <= 32 gains 6-10 % with (2, 3), 120 CTAs
+// against 80; 7B (112 -> 140 CTAs), 72B (128) and 64-token tiles lose.
+void down_cross_cluster_split(int64_t units, int64_t kslices, int mt, const DeviceState* d,
+                              int* splits, int* gsplits) {
+  const int sm_count = d->sm_count;
+  // SWIGLU_DOWN_CLUSTER=s and SWIGLU_DOWN_CLUSTERS=g force the split (for measurements)
+  static const int64_t forced_s = env_int("SWIGLU_DOWN_CLUSTER", 0);
+  static const int64_t forced_g = env_int("SWIGLU_DOWN_CLUSTERS", 0);
+  const auto fits = [&](int s, int g) {
+    return g <= 8 && units * s * g <= sm_count && s * g <= kslices &&
+           (s == 1 || d->small_clusters[s] >= units * g);
+  };
+  if (forced_s > 0 && forced_g > 0) {
+    const int fs = static_cast<int>(forced_s), fg = static_cast<int>(forced_g);
+    if ((fs == 1 || fs == 2 || fs == 4 || fs == 8) && fits(fs, fg)) {
+      *splits = fs;
+      *gsplits = fg;
+    }
+    return;
+  }
+  if (mt > 32) return;
+  const int64_t base = units * *splits;
+  for (int s : {8, 4, 2, 1}) {
+    int g = 0;
+    for (int c = 2; fits(s, c); ++c) g = c;
+    if (g >= 2 && units * s * g * 10 >= base * 14) {
+      *splits = s;
+      *gsplits = g;
+      return;
+    }
+  }
+}
+
+// Bytes of the decode down-projection's workspace for a plan: one counter per
+// (unit, cluster rank), then 2 * mt * 128 fp32 partials per (unit, cluster).
+size_t down_workspace_bytes(const DownPlan& dp) {
+  if (!dp.decode || dp.gsplits <= 1) return 0;
+  const size_t units = size_t(dp.blocks) * size_t(dp.mgroups);
+  const size_t counters = (units * size_t(dp.splits) * 4 + 255) / 256 * 256;
+  return counters + units * size_t(dp.gsplits) * 2 * size_t(dp.mt) * swg::kPackBlockN * 4;
+}
+
+// The down-projection's kernel and launch shape; `cross_cluster` allows the
+// decode kernel's K split across clusters (the call has a workspace).
 swiglu_status_t make_down_plan(int64_t M, int64_t N, int64_t H, const DeviceState* d,
-                               DownPlan* dp) {
+                               DownPlan* dp, bool cross_cluster = false) {
   *dp = DownPlan{};
   dp->blocks = padded_h(H) / 256;  // 256 output columns per block
   const int64_t ks = k_slices(N);
@@ -323,7 +375,11 @@ swiglu_status_t make_down_plan(int64_t M, int64_t N, int64_t H, const DeviceStat
   if (M <= 64 || (M <= swg::kTileM && dp->blocks * 2 <= d->sm_count)) {
     dp->decode = true;
     decode_split_plan(M, dp->blocks, ks, d, &dp->mt, &dp->mgroups, &dp->stages, &dp->splits);
-    dp->grid = static_cast<int>(dp->blocks * dp->mgroups * dp->splits);
+    const int64_t stage_bytes = 2 * swg::kPackBlockN * swg::kBlockK * 2 + int64_t(dp->mt) * 128;
+    if (cross_cluster && dp->mt <= 128 && int64_t(dp->mt) * 1024 <= dp->stages * stage_bytes)
+      down_cross_cluster_split(dp->blocks * dp->mgroups, ks, dp->mt, d, &dp->splits,
+                               &dp->gsplits);
+    dp->grid = static_cast<int>(dp->blocks * dp->mgroups * dp->splits * dp->gsplits);
     return SWIGLU_OK;
   }
   if (d->max_pairs < 1) return SWIGLU_ERR_UNSUPPORTED;
@@ -1167,8 +1223,8 @@ swiglu_status_t swiglu_pack_down_weights(const void* W3, void* W3packed, int64_t
   return SWIGLU_OK;
 }
 
-swiglu_status_t swiglu_down_plan_string(int64_t M, int64_t N, int64_t H, char* buf,
-                                        size_t buflen) {
+static swiglu_status_t down_plan_string(int64_t M, int64_t N, int64_t H, bool cross_cluster,
+                                        char* buf, size_t buflen) {
   if (!buf || buflen == 0) return SWIGLU_ERR_INVALID_ARG;
   buf[0] = '\0';
   swiglu_status_t st = check_shape(M, N, H);
@@ -1177,12 +1233,14 @@ swiglu_status_t swiglu_down_plan_string(int64_t M, int64_t N, int64_t H, char* b
   st = device_state(&d);
   if (st != SWIGLU_OK) return st;
   DownPlan dp;
-  st = make_down_plan(M < 1 ? 1 : M, N, H, d, &dp);
+  st = make_down_plan(M < 1 ? 1 : M, N, H, d, &dp, cross_cluster);
   if (st != SWIGLU_OK) return st;
   if (dp.decode)
-    std::snprintf(buf, buflen, "down small_m mt=%d stages=%d blocks=%lld groups=%d splits=%d grid=%d sms=%d",
+    std::snprintf(buf, buflen,
+                  "down small_m mt=%d stages=%d blocks=%lld groups=%d splits=%d clusters=%d grid=%d "
+                  "sms=%d",
                   dp.mt, dp.stages, static_cast<long long>(dp.blocks), dp.mgroups, dp.splits,
-                  dp.grid, d->sm_count);
+                  dp.gsplits, dp.grid, d->sm_count);
   else
     std::snprintf(buf, buflen, "down large_m_pair tiles=%lld group_m=%lld grid=%d max_pairs=%d sms=%d",
                   static_cast<long long>(dp.tiles), static_cast<long long>(dp.group), dp.grid,
@@ -1190,8 +1248,28 @@ swiglu_status_t swiglu_down_plan_string(int64_t M, int64_t N, int64_t H, char* b
   return SWIGLU_OK;
 }
 
-swiglu_status_t swiglu_down_forward(const void* Y, const void* W3packed, const void* R, void* Out,
-                                    int64_t M, int64_t N, int64_t H, swiglu_stream_t stream) {
+swiglu_status_t swiglu_down_plan_string(int64_t M, int64_t N, int64_t H, char* buf,
+                                        size_t buflen) {
+  return down_plan_string(M, N, H, false, buf, buflen);
+}
+
+swiglu_status_t swiglu_down_plan_string_ws(int64_t M, int64_t N, int64_t H, char* buf,
+                                           size_t buflen) {
+  return down_plan_string(M, N, H, true, buf, buflen);
+}
+
+size_t swiglu_down_workspace_bytes(int64_t M, int64_t N, int64_t H) {
+  if (check_shape(M, N, H) != SWIGLU_OK || M == 0) return 0;
+  DeviceState* d = nullptr;
+  if (device_state(&d) != SWIGLU_OK) return 0;
+  DownPlan dp;
+  if (make_down_plan(M, N, H, d, &dp, true) != SWIGLU_OK) return 0;
+  return down_workspace_bytes(dp);
+}
+
+static swiglu_status_t down_forward(const void* Y, const void* W3packed, const void* R, void* Out,
+                                    int64_t M, int64_t N, int64_t H, void* workspace,
+                                    size_t workspace_bytes, swiglu_stream_t stream) {
   swiglu_status_t st = check_shape(M, N, H);
   if (st != SWIGLU_OK) return st;
   if (M == 0) return SWIGLU_OK;
@@ -1207,8 +1285,17 @@ swiglu_status_t swiglu_down_forward(const void* Y, const void* W3packed, const v
   st = device_state(&d);
   if (st != SWIGLU_OK) return st;
   DownPlan dp;
-  st = make_down_plan(M, N, H, d, &dp);
+  st = make_down_plan(M, N, H, d, &dp, workspace != nullptr);
   if (st != SWIGLU_OK) return st;
+  const size_t ws_bytes = down_workspace_bytes(dp);
+  if (ws_bytes > 0) {  // the plan splits K across clusters: the workspace must hold it
+    if (workspace_bytes < ws_bytes || !aligned16(workspace) ||
+        overlaps(workspace, ws_bytes, Out, size_t(M) * size_t(H) * 2) ||
+        overlaps(workspace, ws_bytes, Y, size_t(M) * size_t(N) * 2) ||
+        overlaps(workspace, ws_bytes, W3packed, swiglu_down_packed_bytes(N, H)) ||
+        (R && overlaps(workspace, ws_bytes, R, size_t(M) * size_t(H) * 2)))
+      return SWIGLU_ERR_INVALID_ARG;
+  }
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t err;
   if (dp.decode) {
@@ -1218,6 +1305,13 @@ swiglu_status_t swiglu_down_forward(const void* Y, const void* W3packed, const v
     p.mgroups = dp.mgroups;
     p.stages = dp.stages;
     p.splits = dp.splits;
+    p.gsplits = dp.gsplits;
+    if (ws_bytes > 0) {  // counters first, then the partials (256-byte aligned)
+      const size_t units = size_t(dp.blocks) * size_t(dp.mgroups);
+      p.counters = static_cast<uint32_t*>(workspace);
+      p.ws = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                      (units * size_t(dp.splits) * 4 + 255) / 256 * 256);
+    }
     if (!encode_2d(&p.tmap_x, Y, N, M, N * 2, swg::kBlockK, p.mt, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_packed_down(&p.tmap_w, W3packed, N, H, 256))
       return SWIGLU_ERR_CUDA;
@@ -1259,6 +1353,18 @@ swiglu_status_t swiglu_down_forward(const void* Y, const void* W3packed, const v
     return SWIGLU_ERR_CUDA;
   }
   return SWIGLU_OK;
+}
+
+swiglu_status_t swiglu_down_forward(const void* Y, const void* W3packed, const void* R, void* Out,
+                                    int64_t M, int64_t N, int64_t H, swiglu_stream_t stream) {
+  return down_forward(Y, W3packed, R, Out, M, N, H, nullptr, 0, stream);
+}
+
+swiglu_status_t swiglu_down_forward_ws(const void* Y, const void* W3packed, const void* R,
+                                       void* Out, int64_t M, int64_t N, int64_t H,
+                                       void* workspace, size_t workspace_bytes,
+                                       swiglu_stream_t stream) {
+  return down_forward(Y, W3packed, R, Out, M, N, H, workspace, workspace_bytes, stream);
 }
 
 void swiglu_testing_inject_stall(int enable, uint32_t timeout_ms) {

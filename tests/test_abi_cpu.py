@@ -109,6 +109,11 @@ def test_valid_call_without_a_device_fails_loudly(native_lib):
     assert lib.swiglu_plan_string(16, 64, 64, 0, buf, 64) == native_lib.SWIGLU_ERR_NO_DEVICE
     assert lib.swiglu_down_plan_string(512, 4096, 1024, buf, 64) == native_lib.SWIGLU_ERR_NO_DEVICE
     assert lib.swiglu_plan_string_fp8(16, 4096, 1024, buf, 64) == native_lib.SWIGLU_ERR_NO_DEVICE
+    assert lib.swiglu_down_plan_string_ws(16, 4096, 1024, buf, 64) == native_lib.SWIGLU_ERR_NO_DEVICE
+    # no device, no plan: no workspace is asked for; a call with one fails like the plain call
+    assert native_lib.swiglu_down_workspace_bytes(16, 4096, 1024) == 0
+    assert lib.swiglu_down_forward_ws(FAKE, FAKE * 64, None, FAKE * 256, 16, 4096, 1024,
+                                      FAKE * 1024, 1 << 20, None) == native_lib.SWIGLU_ERR_NO_DEVICE
 
 
 def test_down_plan_string_checks_arguments_first(native_lib):
@@ -116,6 +121,14 @@ def test_down_plan_string_checks_arguments_first(native_lib):
     buf = ctypes.create_string_buffer(64)
     assert lib.swiglu_down_plan_string(512, 4096, 1024, None, 0) == native_lib.SWIGLU_ERR_INVALID_ARG
     assert lib.swiglu_down_plan_string(512, 4100, 1024, buf, 64) == native_lib.SWIGLU_ERR_UNSUPPORTED
+    assert lib.swiglu_down_plan_string_ws(16, 4096, 1024, None, 0) == native_lib.SWIGLU_ERR_INVALID_ARG
+    assert lib.swiglu_down_plan_string_ws(16, 4100, 1024, buf, 64) == native_lib.SWIGLU_ERR_UNSUPPORTED
+    # shape errors come before any device or workspace check
+    assert native_lib.swiglu_down_workspace_bytes(16, 4100, 1024) == 0
+    assert lib.swiglu_down_forward_ws(FAKE, FAKE * 64, None, FAKE * 256, 16, 4100, 1024,
+                                      FAKE * 1024, 1 << 20, None) == native_lib.SWIGLU_ERR_UNSUPPORTED
+    assert lib.swiglu_down_forward_ws(FAKE, FAKE * 64, None, FAKE * 256, 0, 4096, 1024,
+                                      None, 0, None) == native_lib.SWIGLU_OK
     assert lib.swiglu_plan_string_fp8(16, 4104, 1024, buf, 64) == native_lib.SWIGLU_ERR_UNSUPPORTED
     assert lib.swiglu_plan_string_fp8(16, 4096, 1024, None, 0) == native_lib.SWIGLU_ERR_INVALID_ARG
 
