@@ -57,6 +57,116 @@ constexpr int kMaxClusters = 8;  // K split across at most this many clusters pe
 constexpr size_t kSmemLimit = 232448;
 constexpr int kBarBytes = 256;
 
+// The outputs of token m (of the group starting at m0), weight rows r .. r + 3
+// of column block nblk, from the summed fp32 g and u: SiLU(g) * u (with the
+// FP8 scales), or the two down-projection columns plus the residual.
+template <bool kFp8, bool kDown>
+__device__ __forceinline__ void finish_outputs(const SmallMParams& p, int m0, int nblk, int m,
+                                               int r, float4 g, float4 u) {
+  __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(p.y);
+  if constexpr (kDown) {  // columns n0 + r .. + 3 (g) and n0 + 128 + r .. + 3 (u)
+    const __nv_bfloat16* res = reinterpret_cast<const __nv_bfloat16*>(p.residual);
+    const int n_lo = nblk * 2 * kPackBlockN + r, n_hi = n_lo + kPackBlockN;
+    const size_t row = static_cast<size_t>(m0 + m) * p.N;
+    const float4 parts[2] = {g, u};
+    const int cols[2] = {n_lo, n_hi};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (cols[h] >= p.N) continue;  // N % 8 == 0: cols[h] < N implies cols[h] + 3 < N
+      float4 v = parts[h];
+      if (res) {
+        const uint2 rr = *reinterpret_cast<const uint2*>(res + row + cols[h]);
+        const __nv_bfloat162 r0 = *reinterpret_cast<const __nv_bfloat162*>(&rr.x);
+        const __nv_bfloat162 r1 = *reinterpret_cast<const __nv_bfloat162*>(&rr.y);
+        v.x += __low2float(r0); v.y += __high2float(r0);
+        v.z += __low2float(r1); v.w += __high2float(r1);
+      }
+      uint2 o;
+      o.x = pack_bf16x2(v.x, v.y);
+      o.y = pack_bf16x2(v.z, v.w);
+      *reinterpret_cast<uint2*>(y + row + cols[h]) = o;
+    }
+  } else {
+    const int n = nblk * kPackBlockN + r;  // N % 8 == 0: n < N implies n + 3 < N
+    if (kFp8) {
+      g.x *= p.scale_gate; g.y *= p.scale_gate; g.z *= p.scale_gate; g.w *= p.scale_gate;
+      u.x *= p.scale_up; u.y *= p.scale_up; u.z *= p.scale_up; u.w *= p.scale_up;
+    }
+    if (n < p.N) {
+      uint2 v;
+      v.x = pack_bf16x2(silu_mul(g.x, u.x), silu_mul(g.y, u.y));
+      v.y = pack_bf16x2(silu_mul(g.z, u.z), silu_mul(g.w, u.w));
+      *reinterpret_cast<uint2*>(y + static_cast<size_t>(m0 + m) * p.N + n) = v;
+    }
+  }
+}
+
+// K split across clusters, after this CTA stored its cluster's sums of weight
+// rows [part * R, part * R + R) (R = 128 / splits) in the workspace: count the
+// CTA in on the (unit, rank) counter and, in the last cluster to arrive, add
+// all clusters' sums in cluster order and finish the outputs. Out of line: it
+// runs only with a workspace, and keeps the kernel body small otherwise.
+template <bool kFp8, bool kDown>
+__device__ __noinline__ void cross_cluster_finish(const SmallMParams& p, int unit, int part,
+                                                  int splits, int gsplits, int mt, int mcount,
+                                                  int m0, int nblk, volatile int* last_flag) {
+  const int rows = kPackBlockN / splits;
+  const int chunks = rows / 4;
+  const size_t ws_stride = size_t(2) * mt * kPackBlockN;
+  // Every CTA of every cluster counts itself in exactly once, whatever its
+  // waits returned, so the counter is back at zero when the kernel ends.
+  __syncthreads();  // all of this CTA's partial stores are issued
+  if (threadIdx.x == 0) {
+    __threadfence();  // (cumulative) they are visible before this CTA is counted
+    uint32_t* counter = p.counters + size_t(unit) * splits + part;
+    const uint32_t before = atomicAdd(counter, 1u);
+    const bool last = before == static_cast<uint32_t>(gsplits - 1);
+    if (last) {
+      atomicExch(counter, 0u);  // every cluster of the unit has arrived
+      __threadfence();          // and their partials are visible to this CTA
+    }
+    *last_flag = last ? 1 : 0;
+  }
+  __syncthreads();
+  if (!*last_flag) return;
+  // kSumBatch outputs per thread at a time, the loads of all clusters issued
+  // before the sums (in cluster order: independent of arrival order)
+  constexpr int kSumBatch = 4;
+  const int items = mcount * chunks;
+  for (int i0 = threadIdx.x; i0 < items; i0 += kSumBatch * blockDim.x) {
+    float4 g[kSumBatch], u[kSumBatch];
+#pragma unroll
+    for (int b = 0; b < kSumBatch; ++b) g[b] = u[b] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int c = 0; c < kMaxClusters; ++c) {
+      if (c < gsplits) {
+        const float* src = p.ws + (size_t(unit) * gsplits + c) * ws_stride;
+        float4 gs[kSumBatch], us[kSumBatch];
+#pragma unroll
+        for (int b = 0; b < kSumBatch; ++b) {
+          const int idx = min(i0 + b * static_cast<int>(blockDim.x), items - 1);
+          const int m = idx / chunks;
+          const int r = part * rows + (idx % chunks) * 4;
+          gs[b] = __ldcg(reinterpret_cast<const float4*>(src + size_t(m) * kPackBlockN + r));
+          us[b] = __ldcg(reinterpret_cast<const float4*>(src + size_t(mt + m) * kPackBlockN + r));
+        }
+#pragma unroll
+        for (int b = 0; b < kSumBatch; ++b) {
+          g[b].x += gs[b].x; g[b].y += gs[b].y; g[b].z += gs[b].z; g[b].w += gs[b].w;
+          u[b].x += us[b].x; u[b].y += us[b].y; u[b].z += us[b].z; u[b].w += us[b].w;
+        }
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kSumBatch; ++b) {
+      const int idx = i0 + b * static_cast<int>(blockDim.x);
+      if (idx < items)
+        finish_outputs<kFp8, kDown>(p, m0, nblk, idx / chunks, part * rows + (idx % chunks) * 4,
+                                    g[b], u[b]);
+    }
+  }
+}
+
 template <bool kFp8, bool kDown, bool kMx>
 __global__ void __launch_bounds__(kThreads, 1)
     fused_small_m_kernel(const __grid_constant__ SmallMParams p) {
@@ -329,130 +439,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rows = kPackBlockN / splits;
     const int chunks = rows / 4;
     const uint32_t local = smem_addr(smem);
-    __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(p.y);
-    // the outputs of token m, weight rows r .. r + 3 of the block, from the summed g and u
-    auto finish = [&](int m, int r, float4 g, float4 u) {
-      if constexpr (kDown) {  // columns n0 + r .. + 3 (g) and n0 + 128 + r .. + 3 (u)
-        const __nv_bfloat16* res = reinterpret_cast<const __nv_bfloat16*>(p.residual);
-        const int n_lo = nblk * 2 * kPackBlockN + r, n_hi = n_lo + kPackBlockN;
-        const size_t row = static_cast<size_t>(m0 + m) * p.N;
-        const float4 parts[2] = {g, u};
-        const int cols[2] = {n_lo, n_hi};
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (cols[h] >= p.N) continue;  // N % 8 == 0: cols[h] < N implies cols[h] + 3 < N
-          float4 v = parts[h];
-          if (res) {
-            const uint2 rr = *reinterpret_cast<const uint2*>(res + row + cols[h]);
-            const __nv_bfloat162 r0 = *reinterpret_cast<const __nv_bfloat162*>(&rr.x);
-            const __nv_bfloat162 r1 = *reinterpret_cast<const __nv_bfloat162*>(&rr.y);
-            v.x += __low2float(r0); v.y += __high2float(r0);
-            v.z += __low2float(r1); v.w += __high2float(r1);
-          }
-          uint2 o;
-          o.x = pack_bf16x2(v.x, v.y);
-          o.y = pack_bf16x2(v.z, v.w);
-          *reinterpret_cast<uint2*>(y + row + cols[h]) = o;
-        }
-      } else {
-        const int n = nblk * kPackBlockN + r;  // N % 8 == 0: n < N implies n + 3 < N
-        if (kFp8) {
-          g.x *= p.scale_gate; g.y *= p.scale_gate; g.z *= p.scale_gate; g.w *= p.scale_gate;
-          u.x *= p.scale_up; u.y *= p.scale_up; u.z *= p.scale_up; u.w *= p.scale_up;
-        }
-        if (n < p.N) {
-          uint2 v;
-          v.x = pack_bf16x2(silu_mul(g.x, u.x), silu_mul(g.y, u.y));
-          v.y = pack_bf16x2(silu_mul(g.z, u.z), silu_mul(g.w, u.w));
-          *reinterpret_cast<uint2*>(y + static_cast<size_t>(m0 + m) * p.N + n) = v;
-        }
-      }
-    };
-    // K split across clusters: this cluster's sums, [g rows | u rows] x mt x 128
-    // floats per (unit, cluster)
-    const size_t ws_stride = size_t(2) * mt * kPackBlockN;
-    for (int idx = threadIdx.x; idx < mcount * chunks; idx += blockDim.x) {
-      const int m = idx / chunks;
-      const int r = part * rows + (idx % chunks) * 4;
-      float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
-#pragma unroll 2
-      for (int s = 0; s < splits; ++s) {
-        float4 gs, us;
-        if (splits > 1) {
+    if (gsplits == 1) {
+      // one cluster per unit (splits > 1): sum the cluster's parts and finish
+      for (int idx = threadIdx.x; idx < mcount * chunks; idx += blockDim.x) {
+        const int m = idx / chunks;
+        const int r = part * rows + (idx % chunks) * 4;
+        float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+        for (int s = 0; s < splits; ++s) {
           const uint32_t base = mapa_shared(local, static_cast<uint32_t>(s));
-          gs = ld_shared_cluster_v4(base + 4u * static_cast<uint32_t>(m * kPackBlockN + r));
-          us = ld_shared_cluster_v4(base + 4u * static_cast<uint32_t>((mt + m) * kPackBlockN + r));
-        } else {
-          const float* own = reinterpret_cast<const float*>(smem);
-          gs = *reinterpret_cast<const float4*>(own + m * kPackBlockN + r);
-          us = *reinterpret_cast<const float4*>(own + (mt + m) * kPackBlockN + r);
+          const float4 gs = ld_shared_cluster_v4(base + 4u * static_cast<uint32_t>(m * kPackBlockN + r));
+          const float4 us =
+              ld_shared_cluster_v4(base + 4u * static_cast<uint32_t>((mt + m) * kPackBlockN + r));
+          g.x += gs.x; g.y += gs.y; g.z += gs.z; g.w += gs.w;
+          u.x += us.x; u.y += us.y; u.z += us.z; u.w += us.w;
         }
-        g.x += gs.x; g.y += gs.y; g.z += gs.z; g.w += gs.w;
-        u.x += us.x; u.y += us.y; u.z += us.z; u.w += us.w;
+        finish_outputs<kFp8, kDown>(p, m0, nblk, m, r, g, u);
       }
-      if (gsplits > 1) {
-        float* mine = p.ws + (size_t(unit) * gsplits + gpart) * ws_stride;
+    } else {
+      // K split across clusters: this cluster's sums to the workspace,
+      // [g rows | u rows] x mt x 128 floats per (unit, cluster)
+      float* mine = p.ws + (size_t(unit) * gsplits + gpart) * (size_t(2) * mt * kPackBlockN);
+      for (int idx = threadIdx.x; idx < mcount * chunks; idx += blockDim.x) {
+        const int m = idx / chunks;
+        const int r = part * rows + (idx % chunks) * 4;
+        float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+        for (int s = 0; s < splits; ++s) {
+          float4 gs, us;
+          if (splits > 1) {
+            const uint32_t base = mapa_shared(local, static_cast<uint32_t>(s));
+            gs = ld_shared_cluster_v4(base + 4u * static_cast<uint32_t>(m * kPackBlockN + r));
+            us = ld_shared_cluster_v4(base + 4u * static_cast<uint32_t>((mt + m) * kPackBlockN + r));
+          } else {
+            const float* own = reinterpret_cast<const float*>(smem);
+            gs = *reinterpret_cast<const float4*>(own + m * kPackBlockN + r);
+            us = *reinterpret_cast<const float4*>(own + (mt + m) * kPackBlockN + r);
+          }
+          g.x += gs.x; g.y += gs.y; g.z += gs.z; g.w += gs.w;
+          u.x += us.x; u.y += us.y; u.z += us.z; u.w += us.w;
+        }
         *reinterpret_cast<float4*>(mine + size_t(m) * kPackBlockN + r) = g;
         *reinterpret_cast<float4*>(mine + size_t(mt + m) * kPackBlockN + r) = u;
-      } else {
-        finish(m, r, g, u);
       }
     }
     if (splits > 1) cluster_sync();  // no CTA leaves while a peer may still read its partials
-    if (gsplits > 1) {
-      // Every CTA of every cluster counts itself in exactly once, whatever its
-      // waits returned, so the counter is back at zero when the kernel ends.
-      volatile int* last_flag = abort_flag + 1;
-      __syncthreads();  // all of this CTA's partial stores are issued
-      if (threadIdx.x == 0) {
-        __threadfence();  // (cumulative) they are visible before this CTA is counted
-        uint32_t* counter = p.counters + size_t(unit) * splits + part;
-        const uint32_t before = atomicAdd(counter, 1u);
-        const bool last = before == static_cast<uint32_t>(gsplits - 1);
-        if (last) {
-          atomicExch(counter, 0u);  // every cluster of the unit has arrived
-          __threadfence();          // and their partials are visible to this CTA
-        }
-        *last_flag = last ? 1 : 0;
-      }
-      __syncthreads();
-      if (*last_flag) {
-        // kSumBatch outputs per thread at a time, the loads of all clusters
-        // issued before the sums (in cluster order: independent of arrival order)
-        constexpr int kSumBatch = 4;
-        const int items = mcount * chunks;
-        for (int i0 = threadIdx.x; i0 < items; i0 += kSumBatch * blockDim.x) {
-          float4 g[kSumBatch], u[kSumBatch];
-#pragma unroll
-          for (int b = 0; b < kSumBatch; ++b) g[b] = u[b] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int c = 0; c < kMaxClusters; ++c) {
-            if (c < gsplits) {
-              const float* src = p.ws + (size_t(unit) * gsplits + c) * ws_stride;
-              float4 gs[kSumBatch], us[kSumBatch];
-#pragma unroll
-              for (int b = 0; b < kSumBatch; ++b) {
-                const int idx = min(i0 + b * static_cast<int>(blockDim.x), items - 1);
-                const int m = idx / chunks;
-                const int r = part * rows + (idx % chunks) * 4;
-                gs[b] = __ldcg(reinterpret_cast<const float4*>(src + size_t(m) * kPackBlockN + r));
-                us[b] = __ldcg(reinterpret_cast<const float4*>(src + size_t(mt + m) * kPackBlockN + r));
-              }
-#pragma unroll
-              for (int b = 0; b < kSumBatch; ++b) {
-                g[b].x += gs[b].x; g[b].y += gs[b].y; g[b].z += gs[b].z; g[b].w += gs[b].w;
-                u[b].x += us[b].x; u[b].y += us[b].y; u[b].z += us[b].z; u[b].w += us[b].w;
-              }
-            }
-          }
-#pragma unroll
-          for (int b = 0; b < kSumBatch; ++b) {
-            const int idx = i0 + b * static_cast<int>(blockDim.x);
-            if (idx < items) finish(idx / chunks, part * rows + (idx % chunks) * 4, g[b], u[b]);
-          }
-        }
-      }
-    }
+    if (gsplits > 1)
+      cross_cluster_finish<kFp8, kDown>(p, unit, part, splits, gsplits, mt, mcount, m0, nblk,
+                                        abort_flag + 1);
   }
 
   tc_fence_before();
