@@ -66,12 +66,13 @@ METRIC_DOWN = "MLP down-projection TFLOP/s (2·M·N·H), Out = Y·W3 + R"
 DEFAULT_WORKLOAD = "qwen2.5-72b-prefill-m8192"
 DEFAULT_SECONDARY = "qwen2.5-7b-decode-m16"
 # swiglu_forward_variant's kernel choice (auto = what swiglu_forward does)
-VARIANTS = {"auto": 0, "large": 1, "small": 2, "pair": 3, "sequential": 4, "split": 5}
+VARIANTS = {"auto": 0, "large": 1, "small": 2, "pair": 3, "sequential": 4, "split": 5,
+            "resident": 6}
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = ["swiglu_gated_mlp_gb300/csrc/" + f for f in
                   ("fused_small_m.cu", "fused_large_m.cu", "fused_large_m_pair.cu", "fused_sequential.cu",
-                   "fused_split_k.cu", "ptx.cuh", "kernels.h",
+                   "fused_split_k.cu", "fused_resident_pair.cu", "ptx.cuh", "kernels.h",
                    "swiglu_api.cu")]
 
 
@@ -327,6 +328,7 @@ def prepare(args, sg, w: Workload, dev) -> Prepared:
               "fused_large_m_pair_kernel" if base.startswith("large_m_pair") else
               "fused_sequential_kernel" if base.startswith("sequential") else
               "fused_split_k_kernel" if base.startswith("split_k") else
+              "fused_resident_pair_kernel" if base.startswith("resident_pair") else
               "fused_large_m_kernel")
     if down or fp8:  # the template instance: <fp8> E4M3, <mxfp8> block-scaled, <down>
         kernel += "<down>" if down else "<mxfp8>" if mx else "<fp8>"

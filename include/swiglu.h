@@ -84,9 +84,12 @@ typedef enum {
   SWIGLU_VARIANT_LARGE_M_PAIR = 3, /* 256-token tiles on CTA pairs (tcgen05 cta_group::2) */
   SWIGLU_VARIANT_SEQUENTIAL = 4,   /* gate K loop, then up K loop with SiLU(gate) computed
                                       meanwhile: the pages' Kernel-1 schedule, for comparison */
-  SWIGLU_VARIANT_SPLIT_K = 5       /* 128 x 64 output tiles, each on a cluster of 2 CTAs that
+  SWIGLU_VARIANT_SPLIT_K = 5,      /* 128 x 64 output tiles, each on a cluster of 2 CTAs that
                                       split K and sum their halves in shared memory (small
                                       single-wave problems) */
+  SWIGLU_VARIANT_RESIDENT_PAIR = 6 /* 128 x 64 output tiles on CTA pairs (cta_group::2, M = 128)
+                                      with every K slice loaded at once: K <= 896, bf16;
+                                      UNSUPPORTED otherwise */
 } swiglu_variant_t;
 
 /*

@@ -24,6 +24,7 @@ _EXPORTS = {
     "swiglu_plan_string", "swiglu_testing_inject_stall", "SwigluError",
     "SWIGLU_VARIANT_AUTO", "SWIGLU_VARIANT_LARGE_M", "SWIGLU_VARIANT_SMALL_M",
     "SWIGLU_VARIANT_LARGE_M_PAIR", "SWIGLU_VARIANT_SEQUENTIAL", "SWIGLU_VARIANT_SPLIT_K",
+    "SWIGLU_VARIANT_RESIDENT_PAIR",
 }
 
 

@@ -26,6 +26,7 @@ SWIGLU_VARIANT_SMALL_M = 2
 SWIGLU_VARIANT_LARGE_M_PAIR = 3
 SWIGLU_VARIANT_SEQUENTIAL = 4
 SWIGLU_VARIANT_SPLIT_K = 5
+SWIGLU_VARIANT_RESIDENT_PAIR = 6
 
 PACK_BLOCK_N = 128
 

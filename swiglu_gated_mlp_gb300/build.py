@@ -25,7 +25,7 @@ LIB_PATH = os.path.join(PKG_DIR, "libswiglu.so")
 STAMP = os.path.join(BUILD_DIR, "libswiglu.stamp")
 
 SOURCES = ["swiglu_api.cu", "pack.cu", "fused_large_m.cu", "fused_large_m_pair.cu", "fused_small_m.cu",
-           "fused_sequential.cu", "fused_split_k.cu"]
+           "fused_sequential.cu", "fused_split_k.cu", "fused_resident_pair.cu"]
 HEADERS = ["kernels.h", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",

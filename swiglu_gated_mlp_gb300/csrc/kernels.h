@@ -102,6 +102,13 @@ int split_k_bn();
 int split_k_stages();
 cudaError_t launch_split_k(const LargeMParams& p, cudaStream_t stream);
 
+// Whole K range resident in shared memory (K <= 64 * resident_pair_max_slices()):
+// one 128 x 64 output tile per CTA pair (grid = 2 x tiles), M = 128 MMAs.
+int resident_pair_max_slices();
+int resident_pair_bn();
+cudaError_t configure_resident_pair();
+cudaError_t launch_resident_pair(const LargeMParams& p, cudaStream_t stream);
+
 // Sequential gate-then-up schedule (bn = 128, 128-row tiles), an ablation.
 cudaError_t configure_sequential();
 int sequential_stages();

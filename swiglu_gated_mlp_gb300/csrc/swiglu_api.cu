@@ -27,6 +27,7 @@ struct DeviceState {
   int max_pairs = 0;           // CTA pairs of the pair kernel resident at once
   int small_clusters[9] = {};  // decode-kernel clusters of s CTAs resident at once (s = 2, 4, 8)
   int split_clusters = 0;      // split-K kernel clusters (of 2) resident at once
+  bool resident_pair = false;  // the whole-K-resident pair kernel is set up
   uint32_t* status = nullptr;  // uint32_t[4], see ptx.cuh
 };
 
@@ -142,6 +143,8 @@ swiglu_status_t init_device(int dev, DeviceState& d) {
     cudaGetLastError();
     d.split_clusters = 0;
   }
+  d.resident_pair = swg::configure_resident_pair() == cudaSuccess;
+  if (!d.resident_pair) cudaGetLastError();
   return SWIGLU_OK;
 }
 
@@ -399,7 +402,7 @@ swiglu_status_t make_plan(int64_t M, int64_t K, int64_t N, int variant, const De
   const int sm_count = d ? d->sm_count : 0;
   const int max_pairs = d ? d->max_pairs : 0;
   const int split_clusters = d ? d->split_clusters : 0;
-  if (variant < SWIGLU_VARIANT_AUTO || variant > SWIGLU_VARIANT_SPLIT_K)
+  if (variant < SWIGLU_VARIANT_AUTO || variant > SWIGLU_VARIANT_RESIDENT_PAIR)
     return SWIGLU_ERR_INVALID_ARG;
   const int64_t split_bn = swg::split_k_bn();
   const int64_t split_tiles = ((M + swg::kTileM - 1) / swg::kTileM) * ((N + split_bn - 1) / split_bn);
@@ -433,6 +436,21 @@ swiglu_status_t make_plan(int64_t M, int64_t K, int64_t N, int variant, const De
     // whole grid resident; with few units, K splits over clusters.
     decode_split_plan(M, pl->tiles, kslices, d, &pl->mt, &pl->mgroups, &pl->stages, &pl->splits);
     pl->grid = pl->tiles * pl->mgroups * pl->splits;
+    return SWIGLU_OK;
+  }
+  if (variant == SWIGLU_VARIANT_RESIDENT_PAIR) {
+    // every K slice resident: 128 x 64 tiles, one per CTA pair
+    if (!d || !d->resident_pair || elem_bytes != 2 || kslices > swg::resident_pair_max_slices())
+      return SWIGLU_ERR_UNSUPPORTED;
+    const int64_t bn = swg::resident_pair_bn();
+    const int64_t tm = (M + swg::kTileM - 1) / swg::kTileM, tn = (N + bn - 1) / bn;
+    if (tm * tn > 1073741823) return SWIGLU_ERR_UNSUPPORTED;
+    pl->bn = static_cast<int>(bn);
+    pl->tiles_m = static_cast<int>(tm);
+    pl->tiles_n = static_cast<int>(tn);
+    pl->group_m = 1;
+    pl->tiles = static_cast<int>(tm * tn);
+    pl->grid = 2 * pl->tiles;
     return SWIGLU_OK;
   }
   if (variant == SWIGLU_VARIANT_SPLIT_K) {
@@ -551,9 +569,11 @@ swiglu_status_t launch_forward(const void* A, const void* Wp, void* Y, int64_t M
     err = swg::launch_small_m(p, stream);
   } else {
     swg::LargeMParams p{};
-    if (!encode_2d(&p.tmap_a, A, K, M, K * 2, swg::kBlockK, swg::kTileM,
+    // the whole-K-resident pair kernel: 64 A rows per CTA, 32 gate (up) rows per load
+    const bool resident = pl.variant == SWIGLU_VARIANT_RESIDENT_PAIR;
+    if (!encode_2d(&p.tmap_a, A, K, M, K * 2, swg::kBlockK, resident ? swg::kTileM / 2 : swg::kTileM,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_packed_w(&p.tmap_w, Wp, K, N, pl.bn) ||
+        !encode_packed_w(&p.tmap_w, Wp, K, N, resident ? pl.bn / 2 : pl.bn) ||
         !encode_2d(&p.tmap_y, Y, N, M, N * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
       return SWIGLU_ERR_CUDA;
     p.y = Y;
@@ -572,6 +592,7 @@ swiglu_status_t launch_forward(const void* A, const void* Wp, void* Y, int64_t M
     err = pl.variant == SWIGLU_VARIANT_LARGE_M_PAIR ? swg::launch_large_m_pair(p, stream)
           : pl.variant == SWIGLU_VARIANT_SEQUENTIAL ? swg::launch_sequential(p, stream)
           : pl.variant == SWIGLU_VARIANT_SPLIT_K    ? swg::launch_split_k(p, stream)
+          : resident                                ? swg::launch_resident_pair(p, stream)
                                                     : swg::launch_large_m(p, stream);
   }
   if (err != cudaSuccess) {
@@ -653,6 +674,9 @@ void format_plan(const Plan& pl, const DeviceState& d, const char* prefix, char*
   else if (pl.variant == SWIGLU_VARIANT_SEQUENTIAL)
     std::snprintf(buf, buflen, "%ssequential bn=%d stages=%d tiles=%d grid=%d group_m=%d sms=%d",
                   prefix, pl.bn, pl.stages, pl.tiles, pl.grid, pl.group_m, d.sm_count);
+  else if (pl.variant == SWIGLU_VARIANT_RESIDENT_PAIR)
+    std::snprintf(buf, buflen, "%sresident_pair bn=%d tiles=%d grid=%d sms=%d", prefix, pl.bn,
+                  pl.tiles, pl.grid, d.sm_count);
   else if (pl.variant == SWIGLU_VARIANT_SPLIT_K)
     std::snprintf(buf, buflen, "%ssplit_k bn=%d stages=%d tiles=%d grid=%d clusters=%d sms=%d",
                   prefix, pl.bn, pl.stages, pl.tiles, pl.grid, d.split_clusters, d.sm_count);
@@ -753,7 +777,7 @@ swiglu_status_t swiglu_forward_variant(const void* A, const void* Wpacked, void*
                                        swiglu_stream_t stream) {
   swiglu_status_t st = check_forward_args(A, Wpacked, Y, M, K, N);
   if (st != SWIGLU_OK) return st;
-  if (variant < SWIGLU_VARIANT_AUTO || variant > SWIGLU_VARIANT_SPLIT_K)
+  if (variant < SWIGLU_VARIANT_AUTO || variant > SWIGLU_VARIANT_RESIDENT_PAIR)
     return SWIGLU_ERR_INVALID_ARG;
   if (M == 0) return SWIGLU_OK;
   DeviceState* d = nullptr;

@@ -81,7 +81,7 @@ def test_forward_rejects_null_misaligned_and_aliased(native_lib):
 
 def test_forward_variant_rejects_unknown_variant(native_lib):
     lib = native_lib.lib
-    for bad in (-1, 6, 99):
+    for bad in (-1, 7, 99):
         assert lib.swiglu_forward_variant(FAKE, FAKE * 64, FAKE * 256, 4, 64, 64, bad, None) == 1
 
 

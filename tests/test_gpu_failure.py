@@ -26,7 +26,8 @@ def native(native_lib):
     return native_lib
 
 
-@pytest.mark.parametrize("variant,M", [(1, 64), (2, 16), (1, 300), (3, 300), (4, 200), (5, 128)])
+@pytest.mark.parametrize("variant,M", [(1, 64), (2, 16), (1, 300), (3, 300), (4, 200), (5, 128),
+                                       (6, 128)])
 def test_stalled_pipeline_reports_timeout_and_context_survives(native, variant, M):
     K, N = 256, 384
     a, w1, w2 = make_inputs(M, K, N, seed=5)

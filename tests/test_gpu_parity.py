@@ -18,7 +18,7 @@ from gpu_helpers import (check_against_oracle, run_forward, sentinel_buffer, sen
 
 pytestmark = pytest.mark.gpu
 
-AUTO, LARGE, SMALL, PAIR, SEQ, SPLIT = 0, 1, 2, 3, 4, 5
+AUTO, LARGE, SMALL, PAIR, SEQ, SPLIT, RESIDENT = 0, 1, 2, 3, 4, 5, 6
 
 
 @pytest.fixture(scope="module")
@@ -119,6 +119,27 @@ def test_split_k_kernel_matches_oracle(native, M, K, N):
     check_against_oracle(native, M, K, N, seed=M * 19 + K + N, variant=SPLIT)
 
 
+# Every K slice resident in shared memory (K <= 896): 128 x 64 tiles on CTA
+# pairs with M = 128 MMAs; the 0.5B shape, ragged M, K and N, more tiles than
+# SMs, a single K slice.
+RESIDENT_CASES = [(128, 896, 4864), (100, 200, 264), (1, 64, 128), (129, 136, 256),
+                  (300, 512, 1000), (65, 896, 520), (257, 832, 4864), (90, 8, 8), (64, 72, 64)]
+
+
+@pytest.mark.parametrize("M,K,N", RESIDENT_CASES)
+def test_resident_pair_kernel_matches_oracle(native, M, K, N):
+    assert native.swiglu_plan_string(M, K, N, RESIDENT).startswith("resident_pair"), (M, K, N)
+    check_against_oracle(native, M, K, N, seed=M * 23 + K + N, variant=RESIDENT)
+
+
+def test_resident_pair_rejects_long_k(native):
+    # K = 960 needs 15 slices: more than shared memory holds at once
+    a, w1, w2 = make_inputs(16, 960, 128, seed=3)
+    with pytest.raises(native.SwigluError) as err:
+        run_forward(native, a, w1, w2, RESIDENT)
+    assert err.value.code == native.SWIGLU_ERR_UNSUPPORTED
+
+
 # The pages' Kernel-1 schedule (gate K loop, then up K loop), kept for comparison.
 SEQ_CASES = [(1, 64, 128), (100, 200, 264), (129, 136, 256), (300, 512, 1000), (513, 896, 4864),
              (2048, 128, 2048)]
@@ -134,7 +155,7 @@ def test_auto_choice_matches_oracle(native, M, K, N):
     check_against_oracle(native, M, K, N, seed=M + K + N, variant=AUTO)
 
 
-@pytest.mark.parametrize("variant", [LARGE, SMALL, PAIR, SEQ, SPLIT])
+@pytest.mark.parametrize("variant", [LARGE, SMALL, PAIR, SEQ, SPLIT, RESIDENT])
 def test_variants_agree(native, variant):
     # both kernels accumulate in fp32; their bf16 outputs agree within 1 ulp-ish
     a, w1, w2 = make_inputs(48, 640, 512, seed=77)
@@ -149,7 +170,7 @@ def test_variants_agree(native, variant):
 TOKEN_COUNTS = list(range(1, 18)) + [127, 128, 129]
 
 
-@pytest.mark.parametrize("variant", [AUTO, SMALL, LARGE, PAIR, SPLIT])
+@pytest.mark.parametrize("variant", [AUTO, SMALL, LARGE, PAIR, SPLIT, RESIDENT])
 @pytest.mark.parametrize("M", TOKEN_COUNTS)
 def test_every_small_token_count_matches_oracle(native, M, variant):
     check_against_oracle(native, M, 200, 264, seed=1000 + M, variant=variant)
@@ -183,7 +204,7 @@ def test_largest_k_and_n_match_oracle(native, M, K, N):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("variant", [AUTO, LARGE, SMALL, PAIR, SEQ, SPLIT])
+@pytest.mark.parametrize("variant", [AUTO, LARGE, SMALL, PAIR, SEQ, SPLIT, RESIDENT])
 @pytest.mark.parametrize("M", [1, 9, 130])
 def test_smallest_k_and_n_match_oracle(native, variant, M):
     check_against_oracle(native, M, 8, 8, seed=M + variant, variant=variant)
