@@ -40,6 +40,12 @@ struct LargeCfg {
   static constexpr int kBBytes = 2 * BN * kBlockK * 2;   // BN gate rows + BN up rows
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = (BN == 128) ? 4 : ((BN == 64) ? 6 : 8);
+  // Ring slots handed over per full/empty barrier exchange: with 32-column
+  // tiles (small problems, whose time goes to per-stage hand-offs rather than
+  // to bytes) two 64-deep K slices at a time; deeper slices would leave the
+  // shallower rings of the wider tiles too few exchanges in flight.
+  static constexpr int kSlots = (BN == 32) ? 2 : 1;
+  static_assert(kStages % kSlots == 0, "ring slots per exchange");
   static constexpr int kAccCols = 2 * BN;                // fp32 TMEM columns per accumulator
   static constexpr int kTmemCols = 2 * kAccCols;         // double buffered (128, 256 or 512)
   static constexpr int kStoreCols = 32;                  // output columns per TMA store
@@ -154,7 +160,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // inside the 256-row tile; the matching up rows follow 128 later
         const int wtile = (col0 / kPackBlockN) * num_kb;
         const int wrow = col0 % kPackBlockN;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        // kSlots consecutive slots (K slices) per exchange on slot s's barriers
+        for (int kb = 0; kb < num_kb; kb += C::kSlots) {
           if (!mbar_wait(empty0 + 8u * s, ph ^ 1u, wc, kSiteProducerEmpty)) {
             ok = false;
             break;
@@ -163,16 +170,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             skip_once = false;  // testing hook: leave this stage unfilled
           } else {
             const uint32_t fb = full0 + 8u * s;
-            const int k0 = kb * kBlockK;
-            mbar_arrive_expect_tx(fb, C::kStageBytes);
-            tma_load_2d(sA + s * C::kABytes, &p.tmap_a, fb, k0, m0);
-            tma_load_3d(sB + s * C::kBBytes, &p.tmap_w, fb, 0, wrow, wtile + kb);
-            tma_load_3d(sB + s * C::kBBytes + BN * kBlockK * 2, &p.tmap_w, fb, 0,
-                        wrow + kPackBlockN, wtile + kb);
+            const int na = min(C::kSlots, num_kb - kb);
+            mbar_arrive_expect_tx(fb, na * C::kStageBytes);
+            for (int a = 0; a < na; ++a) {
+              const int ss = s + a, k0 = (kb + a) * kBlockK;
+              tma_load_2d(sA + ss * C::kABytes, &p.tmap_a, fb, k0, m0);
+              tma_load_3d(sB + ss * C::kBBytes, &p.tmap_w, fb, 0, wrow, wtile + kb + a);
+              tma_load_3d(sB + ss * C::kBBytes + BN * kBlockK * 2, &p.tmap_w, fb, 0,
+                          wrow + kPackBlockN, wtile + kb + a);
+            }
             filled |= 1u << s;
             fill_ph = (fill_ph & ~(1u << s)) | (ph << s);
           }
-          if (++s == C::kStages) {
+          s += C::kSlots;
+          if (s == C::kStages) {
             s = 0;
             ph ^= 1u;
           }
@@ -197,19 +208,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(tempty0 + 8u * buf, acc_ph ^ 1u, wc, kSiteMmaTmemEmpty)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + buf * C::kAccCols;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = 0; kb < num_kb; kb += C::kSlots) {
           if (!mbar_wait(full0 + 8u * s, ph, wc, kSiteMmaFull)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t adesc = smem_desc_sw128(sA + s * C::kABytes);
-          const uint64_t bdesc = smem_desc_sw128(sB + s * C::kBBytes);
+          const int na = min(C::kSlots, num_kb - kb);
+          for (int a = 0; a < na; ++a) {
+            const uint64_t adesc = smem_desc_sw128(sA + (s + a) * C::kABytes);
+            const uint64_t bdesc = smem_desc_sw128(sB + (s + a) * C::kBBytes);
 #pragma unroll
-          for (int k = 0; k < kBlockK / 16; ++k)
-            mma_bf16(d, adesc + 2u * k, bdesc + 2u * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
-          mma_commit(empty0 + 8u * s);  // frees the stage once these MMAs have read it
-          if (++s == C::kStages) {
+            for (int k = 0; k < kBlockK / 16; ++k)
+              mma_bf16(d, adesc + 2u * k, bdesc + 2u * k, kIdesc, ((kb + a) | k) != 0 ? 1u : 0u);
+          }
+          mma_commit(empty0 + 8u * s);  // frees the slots once these MMAs have read them
+          s += C::kSlots;
+          if (s == C::kStages) {
             s = 0;
             ph ^= 1u;
           }
