@@ -43,8 +43,15 @@
  *                           its grid-dependency wait (default: about 64 MB
  *                           over the grid, at most 16 per CTA; 4 in K-split
  *                           clusters).
+ *   SWIGLU_L2_PREFETCH_LARGE=n  K slices each single-CTA kernel CTA stages in
+ *                           L2 before its grid-dependency wait, for long K
+ *                           loops (default: about 64 MB over the grid).
  *   SWIGLU_PAIR_GROUP_M=g   row tiles per group in the CTA-pair kernels' tile
  *                           order (default 16).
+ *   SWIGLU_DOWN_CLUSTER=s, SWIGLU_DOWN_CLUSTERS=g  (both set) the decode
+ *                           down-projection's K split with a workspace: g
+ *                           clusters of s CTAs per output block, where they fit
+ *                           (default: the measured rule of swiglu_down_forward_ws).
  *   SWIGLU_VERBOSE=1        swiglu_check_device_status prints the status record
  *                           (wait site, block, count) to stderr on a failure.
  */
