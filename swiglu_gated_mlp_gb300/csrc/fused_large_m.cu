@@ -113,7 +113,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 2 && lane == 0 && p.l2_prefetch > 0 && num_kb >= 4 * C::kStages &&
+  // L2 staging of the first K slices before the grid-dependency wait: for long
+  // K loops (at least 4 ring-fulls) p.l2_prefetch slices, and with 32-column
+  // tiles (small problems) the first 4 (on the 0.5B shape 4 measured 2 %
+  // faster than none; 8 and all 14 slower).
+  const bool long_k = num_kb >= 4 * C::kStages;
+  if (warp == 2 && lane == 0 && p.l2_prefetch > 0 && (long_k || BN == 32) &&
       static_cast<int>(blockIdx.x) < num_tiles) {
     // Inputs of the step, not products of the kernel before it in the stream;
     // L2 is coherent, so loads after the wait still see any write that kernel
@@ -124,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wtile = (col0 / kPackBlockN) * num_kb;
     const int wrow = col0 % kPackBlockN;
     const uint64_t pol = policy_evict_first();
-    const int nw = min(p.l2_prefetch, num_kb);
+    const int nw = min(long_k ? p.l2_prefetch : 4, num_kb);
     for (int kb = 0; kb < nw; ++kb) {
       tma_prefetch_l2_3d_hint(&p.tmap_w, 0, wrow, wtile + kb, pol);
       tma_prefetch_l2_3d_hint(&p.tmap_w, 0, wrow + kPackBlockN, wtile + kb, pol);
