@@ -31,6 +31,7 @@ N > 1 runs independent replicas (the op has no exchange step), one per rank.
 from __future__ import annotations
 
 import os
+import re
 
 # BLAS threads of the CPU oracle: the cores this process may run on.
 _CORES = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
@@ -93,11 +94,19 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback (no MEASURED_PEAKS.json)"
 
 
+def _code_only(text: str) -> str:
+    """C++/CUDA source without comments and blank lines (comment edits keep the stamp)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*", "", line).rstrip() for line in text.splitlines())
+    return "\n".join(line for line in lines if line)
+
+
 def source_stamp() -> str:
+    """Hash of the kernel sources' code (comments and blank lines left out)."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -21,13 +21,16 @@
 //    staging -> TMA store) overlaps the MMAs of tile i+1;
 //  * every pipeline wait is bounded (see ptx.cuh); a stuck wait aborts the
 //    CTA cleanly and is reported through the status word;
-//  * on long K loops (at least 4 ring-fulls) an idle epilogue warp asks L2,
-//    before the grid-dependency wait, to fetch the first packed weight slices
-//    of the CTA's first tile (about 64 MB over the grid) and a share of its A
-//    rows, so the first DRAM reads start under the previous grid's tail. On
-//    short loops (the 0.5B shape: 14 slices, 8 stages) staging measured
-//    slower, both before the wait and right after the first ring-full, so it
-//    is off there.
+//  * before the grid-dependency wait an idle epilogue warp asks L2 to fetch
+//    the first packed weight slices of the CTA's first tile and a share of
+//    its A rows, so the first DRAM reads start under the previous grid's
+//    tail: on long K loops (at least 4 ring-fulls) about 64 MB over the grid,
+//    with 32-column tiles (small problems) the first 4 slices (more measured
+//    slower there, as did staging right after the first ring-full);
+//  * with 32-column tiles the producer and the MMA issuer hand over two K
+//    slices per full/empty barrier exchange: small problems (the 0.5B shape,
+//    14 slices in an 8-slot ring) wait on these hand-offs rather than on
+//    bytes, and two per exchange took that shape from 7.39 to 6.94 us.
 #include "kernels.h"
 #include "ptx.cuh"
 

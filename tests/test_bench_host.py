@@ -108,3 +108,16 @@ def test_profiled_traffic_reads_both_record_forms(tmp_path, monkeypatch):
     assert bench.profiled_traffic("k_b<fp8>", "w1")[0] == 200.0
     assert bench.profiled_traffic("k_b<fp8>", "w2") == (None, None)  # stale stamp
     assert bench.profiled_traffic("k_a", "w2") == (None, None)
+
+
+def test_source_stamp_ignores_comments_not_code(tmp_path, monkeypatch):
+    src = tmp_path / "k.cu"
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "KERNEL_SOURCES", ["k.cu"])
+    src.write_text("int f(int x) {  // doubles x\n  return 2 * x;\n}\n")
+    base = bench.source_stamp()
+    src.write_text("/* a block\n   comment */\nint f(int x) {  // twice x\n\n  return 2 * x;\n}\n")
+    assert bench.source_stamp() == base  # comments and blank lines only
+    src.write_text("int f(int x) {  // doubles x\n  return 3 * x;\n}\n")
+    assert bench.source_stamp() != base  # a code change
+    assert bench._code_only("a = 1;  // c\n/* x */ b = 2;\n") == "a = 1;\n b = 2;"
