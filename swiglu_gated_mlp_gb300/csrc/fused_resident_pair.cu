@@ -25,6 +25,12 @@
 // One tile per CTA pair (the grid holds every tile at once): the even CTA's
 // "full" barriers count both CTAs' bytes (cta_group::2 loads), its MMA commit
 // arrives on both CTAs' "accumulator full" barrier, and every wait is bounded.
+//
+// Measured on GB300 it is slower than the single-CTA kernel on the 0.5B shape
+// (8.4 against 6.9 us): timing copies of that kernel showed the shape waiting
+// on per-slice pipeline hand-offs and small MMAs rather than on the second
+// round trip, and the M = 128 pair MMAs here follow the loads. It is a
+// selectable variant (SWIGLU_VARIANT_RESIDENT_PAIR), not an automatic choice.
 #include "kernels.h"
 #include "ptx.cuh"
 

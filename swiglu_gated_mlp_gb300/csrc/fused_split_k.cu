@@ -25,6 +25,11 @@
 //  * every pipeline wait is bounded (ptx.cuh); every thread of both CTAs
 //    reaches both cluster barriers whatever the waits returned, so a CTA
 //    whose wait ran out never leaves its peer waiting.
+//
+// Measured on GB300 it is slower than the single-CTA kernel on the 0.5B shape
+// (8.0 against 7.35 us before that kernel's two-slice exchanges): the round
+// trip it saves is not what that shape waits on. It is a selectable variant
+// (SWIGLU_VARIANT_SPLIT_K), not an automatic choice.
 #include "kernels.h"
 #include "ptx.cuh"
 
