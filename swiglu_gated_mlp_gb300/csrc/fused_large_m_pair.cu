@@ -21,6 +21,21 @@
 //    barriers (multicast commit); both epilogues arrive on rank 0's
 //    "accumulator empty" barrier; every wait is bounded (ptx.cuh).
 //
+// Tile rounds are kept loosely in step across the pairs: pair p takes tiles
+// p, p + pairs, p + 2 pairs, ... (round 0, 1, 2, ...), and the tiles of one
+// round share A rows and weight columns through L2 only while the pairs are
+// near each other. Left alone, pairs drift apart by whole rounds over a long
+// run (the 72B prefill read its operands 7-11 times over from DRAM), so the
+// even CTA's producer, before the loads of its round r tile, waits until every
+// pair has issued all loads of its round r - 2 tile (a per-round counter in
+// global memory, tagged with a launch number the CTAs draw on the device, so
+// graph replays count apart). Every such wait is bounded and, if it runs out,
+// only turns pacing off for the rest of the launch; results never depend on
+// it. Paced are bf16 gate/up launches with K >= 8192 (long tiles; the 72B
+// prefill): DRAM reads 11.0-13.4 -> 7.9-8.8 GB per launch at the same time
+// (lag 1: much slower; lag 4: more reads). Shorter tiles lose time when
+// paced, since the slowest pair of each round then sets everyone's pace.
+//
 // With kDown the same pipeline computes the MLP's down-projection
 // Out = Y x W3 + R: a tile is 256 consecutive output columns (rank r loads
 // packed rows [128 r, 128 r + 128) of W3's tile), and the epilogue stores
@@ -85,6 +100,39 @@ __device__ __forceinline__ void pair_tile_coords(int t, int tiles_m, int tiles_n
   const int r = t - g * per_group;
   mb = first_m + r % gm;
   nb = r / gm;
+}
+
+// Round pacing state (see the head of this file): launch numbers are drawn
+// from g_pace_ticket by the even CTA of every pair; g_pace_round[r] holds
+// (launch number << 32) | pairs that issued all loads of their round r tile.
+constexpr int kPaceLag = 2;
+constexpr int kPaceRounds = 1024;               // rounds beyond this are not paced
+constexpr uint64_t kPaceWaitNs = 200000;        // one wait's limit: then pacing stops
+constexpr int kPaceMinSlices = 128;             // paced only with K >= 128 slices of 64
+__device__ unsigned int g_pace_ticket;
+__device__ unsigned long long g_pace_round[kPaceRounds];
+
+// Waits (bounded) until `need` pairs of launch `epoch` counted themselves in
+// round r; false if the wait ran out or a later launch owns the counter.
+__device__ __forceinline__ bool pace_wait(int r, unsigned long long epoch, unsigned need) {
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    const unsigned long long v = *reinterpret_cast<volatile unsigned long long*>(&g_pace_round[r]);
+    if ((v >> 32) == epoch && static_cast<unsigned>(v & 0xffffffffull) >= need) return true;
+    if ((v >> 32) > epoch || globaltimer_ns() - t0 > kPaceWaitNs) return false;
+  }
+}
+
+// Counts this pair in for round r of launch `epoch` (a counter left by
+// another launch restarts at 1).
+__device__ __forceinline__ void pace_count(int r, unsigned long long epoch) {
+  unsigned long long* c = &g_pace_round[r];
+  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(c), assumed;
+  do {
+    assumed = old;
+    const unsigned long long next = (assumed >> 32) == epoch ? assumed + 1ull : (epoch << 32) | 1ull;
+    old = atomicCAS(c, assumed, next);
+  } while (old != assumed);
 }
 
 template <bool kFp8, bool kDown, bool kMx>
@@ -167,7 +215,23 @@ __global__ void __launch_bounds__(PairCfg<kMx>::kThreadsT, 1)
       uint32_t filled = 0, fill_ph = 0;
       bool skip_once = p.inject_stall != 0;
       bool ok = true;
-      for (int t = pair; ok && t < num_tiles; t += pairs) {
+      // round pacing on the even CTA (the odd one follows through the empty
+      // barriers); the launch number is drawn after the grid-dependency wait,
+      // when the previous launch in the stream has finished
+      const unsigned long long epoch =
+          leader ? static_cast<unsigned long long>(atomicAdd(&g_pace_ticket, 1u) / unsigned(pairs)) + 1ull
+                 : 0ull;
+      // only long bf16 gate/up tiles (K >= 8192, the 72B shape): with shorter
+      // tiles the slowest pair of each round sets everyone's pace (7B prefill
+      // +30 %, FP8 72B +13 %, block-scaled 7B +73 % when paced)
+      const bool paced = leader && !kFp8 && !kDown && num_kb >= kPaceMinSlices;
+      bool pacing = paced;  // off for the rest of the launch once a wait runs out
+      int round = 0;
+      for (int t = pair; ok && t < num_tiles; t += pairs, ++round) {
+        if (pacing && round >= kPaceLag && round - kPaceLag < kPaceRounds) {
+          const int r = round - kPaceLag;
+          pacing = pace_wait(r, epoch, static_cast<unsigned>(min(pairs, num_tiles - r * pairs)));
+        }
         int mb, nb;
         pair_tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, mb, nb);
         const int m0 = mb * 2 * kTileM + static_cast<int>(rank) * kTileM;
@@ -201,6 +265,7 @@ __global__ void __launch_bounds__(PairCfg<kMx>::kThreadsT, 1)
             ph ^= 1u;
           }
         }
+        if (paced && ok && round < kPaceRounds) pace_count(round, epoch);
       }
       pdl_launch_dependents();
       // Rank 0's full barriers count both CTAs' bytes: once they complete, every

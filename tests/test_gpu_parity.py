@@ -346,3 +346,32 @@ def test_plan_string_names_a_kernel(native):
     assert native.swiglu_plan_string(16, 3584, 18944).startswith("small_m")
     assert native.swiglu_plan_string(4096, 3584, 18944).startswith("large_m_pair bn=128")
     assert native.swiglu_plan_string(4096, 3584, 18944, 1).startswith("large_m bn=128")
+
+
+def test_pair_kernel_launches_on_two_streams_at_once(native):
+    # The pair kernel keeps its tile rounds loosely in step through per-round
+    # counters in global memory, tagged per launch (bf16, K >= 8192). Two
+    # launches in flight at once (separate streams) share those counters: each
+    # must still give the oracle's result (their pacing waits run out and
+    # stop; nothing else depends on them). 1024 x 8192 outputs: 256 tiles,
+    # about 3.4 rounds a pair, so the waits from round 2 on are exercised.
+    from oracle import compare
+    from swiglu_gated_mlp_gb300.workloads import sample_rows
+    M, K, N = 1024, 8192, 8192
+    inputs = [make_inputs(M, K, N, seed=31 + i) for i in range(2)]
+    dev = [tuple(t.cuda() for t in x) for x in inputs]
+    wps = [native.swiglu_pack_weights(w1, w2) for _, w1, w2 in dev]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    ys = [torch.empty(M, N, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    torch.cuda.synchronize()
+    for _ in range(4):
+        for i in range(2):
+            native.swiglu_forward_variant(dev[i][0], wps[i], N, PAIR, Y=ys[i], stream=streams[i])
+    torch.cuda.synchronize()
+    native.swiglu_check_device_status()
+    rows = sample_rows(M, 64, seed=5)
+    for i in range(2):
+        a, w1, w2 = inputs[i]
+        ref = swiglu_f64(bf16_bits(a), bf16_bits(w1), bf16_bits(w2), rows=rows)
+        rep = compare.report(bf16_bits(ys[i].cpu())[rows], ref)
+        assert rep["nonfinite"] == 0 and rep["tolerance_pass"], rep
