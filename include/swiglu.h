@@ -378,7 +378,7 @@ SWIGLU_API swiglu_status_t swiglu_down_plan_string_ws(int64_t M, int64_t N, int6
  * synchronises (page-locked memory keeps the copy asynchronous; pageable
  * memory makes the call wait for the kernel).
  * The first call on a device does a one-time set-up (kernel attributes and the
- * array's device address); make that first call before any stream capture.
+ * array's device address, both host-side CUDA runtime queries).
  * Calls whose kernels overlap on the GPU (several streams) share the record
  * and race on it; serialise them to get a meaningful status.
  */
