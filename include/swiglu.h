@@ -394,6 +394,18 @@ SWIGLU_API swiglu_status_t swiglu_forward_noalloc(const void* A, const void* Wpa
  */
 SWIGLU_API void swiglu_testing_inject_stall(int enable, uint32_t timeout_ms);
 
+/*
+ * Testing counter of the CTA-pair kernel's tile-round pacing (bf16 gate/up,
+ * K >= 8192: each pair waits, bounded, for every pair of the launch to have
+ * issued the loads of the tile two rounds back; a wait that runs out only
+ * turns pacing off for the rest of that launch). Writes to `*count` (HOST)
+ * the number of such waits that ran out on the current device since the
+ * library was loaded. Synchronous with the device (reads a device counter).
+ * No passage of the method defines it: it is test infrastructure of the
+ * boundary. Errors: INVALID_ARG (count NULL), NO_DEVICE, CUDA.
+ */
+SWIGLU_API swiglu_status_t swiglu_testing_pace_run_out(uint64_t* count);
+
 #ifdef __cplusplus
 }
 #endif

@@ -21,7 +21,8 @@ _EXPORTS = {
     "swiglu_down_forward", "swiglu_down_plan_string", "swiglu_plan_string_fp8",
     "swiglu_down_workspace_bytes", "swiglu_down_workspace", "swiglu_down_plan_string_ws",
     "swiglu_packed_weight_bytes", "swiglu_check_device_status", "swiglu_status_string",
-    "swiglu_plan_string", "swiglu_testing_inject_stall", "SwigluError",
+    "swiglu_plan_string", "swiglu_testing_inject_stall", "swiglu_testing_pace_run_out",
+    "SwigluError",
     "SWIGLU_VARIANT_AUTO", "SWIGLU_VARIANT_LARGE_M", "SWIGLU_VARIANT_SMALL_M",
     "SWIGLU_VARIANT_LARGE_M_PAIR", "SWIGLU_VARIANT_SEQUENTIAL", "SWIGLU_VARIANT_SPLIT_K",
     "SWIGLU_VARIANT_RESIDENT_PAIR",

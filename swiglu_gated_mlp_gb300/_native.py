@@ -93,6 +93,8 @@ lib.swiglu_forward_noalloc.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp
 lib.swiglu_forward_noalloc.restype = _int
 lib.swiglu_testing_inject_stall.argtypes = [_int, _u32]
 lib.swiglu_testing_inject_stall.restype = None
+lib.swiglu_testing_pace_run_out.argtypes = [ctypes.POINTER(ctypes.c_uint64)]
+lib.swiglu_testing_pace_run_out.restype = _int
 
 
 class SwigluError(RuntimeError):
@@ -538,3 +540,10 @@ def swiglu_plan_string(M: int, K: int, N: int, variant: int = SWIGLU_VARIANT_AUT
 
 def swiglu_testing_inject_stall(enable: bool, timeout_ms: int = 0) -> None:
     lib.swiglu_testing_inject_stall(1 if enable else 0, int(timeout_ms))
+
+
+def swiglu_testing_pace_run_out() -> int:
+    """Pacing waits of the CTA-pair kernel that ran out on the current device."""
+    v = ctypes.c_uint64(0)
+    _check(lib.swiglu_testing_pace_run_out(ctypes.byref(v)), "swiglu_testing_pace_run_out")
+    return v.value

@@ -29,9 +29,11 @@
 // even CTA's producer, before the loads of its round r tile, waits until every
 // pair has issued all loads of its round r - 2 tile (a per-round counter in
 // global memory, tagged with a launch number the CTAs draw on the device, so
-// graph replays count apart). Every such wait is bounded and, if it runs out,
-// only turns pacing off for the rest of the launch; results never depend on
-// it. Paced are bf16 gate/up launches with K >= 8192 (long tiles; the 72B
+// graph replays count apart: every launch takes one block of kPaceBlock
+// numbers from a global ticket, pair 0 all but pairs - 1 of them, so blocks
+// stay aligned whatever the grid sizes of earlier launches). Every such wait
+// is bounded and, if it runs out, only turns pacing off for the rest of the
+// launch; results never depend on it. Paced are bf16 gate/up launches with K >= 8192 (long tiles; the 72B
 // prefill): DRAM reads 11.0-13.4 -> 7.9-8.8 GB per launch at the same time
 // (lag 1: much slower; lag 4: more reads). Shorter tiles lose time when
 // paced, since the slowest pair of each round then sets everyone's pace.
@@ -102,15 +104,18 @@ __device__ __forceinline__ void pair_tile_coords(int t, int tiles_m, int tiles_n
   nb = r / gm;
 }
 
-// Round pacing state (see the head of this file): launch numbers are drawn
-// from g_pace_ticket by the even CTA of every pair; g_pace_round[r] holds
-// (launch number << 32) | pairs that issued all loads of their round r tile.
+// Round pacing state (see the head of this file): the even CTA of every pair
+// draws from g_pace_ticket, launch number = ticket / kPaceBlock + 1 (32 bits);
+// g_pace_round[r] holds (launch number << 32) | pairs that issued all loads of
+// their round r tile; g_pace_run_out counts waits that ran out (testing).
 constexpr int kPaceLag = 2;
 constexpr int kPaceRounds = 1024;               // rounds beyond this are not paced
 constexpr uint64_t kPaceWaitNs = 200000;        // one wait's limit: then pacing stops
 constexpr int kPaceMinSlices = 128;             // paced only with K >= 128 slices of 64
-__device__ unsigned int g_pace_ticket;
+constexpr unsigned long long kPaceBlock = 1024;  // tickets per launch (>= pairs)
+__device__ unsigned long long g_pace_ticket;
 __device__ unsigned long long g_pace_round[kPaceRounds];
+__device__ unsigned long long g_pace_run_out;
 
 // Waits (bounded) until `need` pairs of launch `epoch` counted themselves in
 // round r; false if the wait ran out or a later launch owns the counter.
@@ -119,7 +124,11 @@ __device__ __forceinline__ bool pace_wait(int r, unsigned long long epoch, unsig
   for (;;) {
     const unsigned long long v = *reinterpret_cast<volatile unsigned long long*>(&g_pace_round[r]);
     if ((v >> 32) == epoch && static_cast<unsigned>(v & 0xffffffffull) >= need) return true;
-    if ((v >> 32) > epoch || globaltimer_ns() - t0 > kPaceWaitNs) return false;
+    if ((v >> 32) > epoch) return false;
+    if (globaltimer_ns() - t0 > kPaceWaitNs) {
+      atomicAdd(&g_pace_run_out, 1ull);
+      return false;
+    }
   }
 }
 
@@ -217,14 +226,18 @@ __global__ void __launch_bounds__(PairCfg<kMx>::kThreadsT, 1)
       bool ok = true;
       // round pacing on the even CTA (the odd one follows through the empty
       // barriers); the launch number is drawn after the grid-dependency wait,
-      // when the previous launch in the stream has finished
-      const unsigned long long epoch =
-          leader ? static_cast<unsigned long long>(atomicAdd(&g_pace_ticket, 1u) / unsigned(pairs)) + 1ull
-                 : 0ull;
+      // when the previous launch in the stream has finished. The launch's
+      // draws add up to kPaceBlock, so the next launch starts a fresh block.
+      const bool can_pace = pairs <= static_cast<int>(kPaceBlock);
+      unsigned long long epoch = 0;
+      if (leader && can_pace) {
+        const unsigned long long take = pair == 0 ? kPaceBlock - static_cast<unsigned long long>(pairs - 1) : 1ull;
+        epoch = ((atomicAdd(&g_pace_ticket, take) / kPaceBlock) + 1ull) & 0xffffffffull;
+      }
       // only long bf16 gate/up tiles (K >= 8192, the 72B shape): with shorter
       // tiles the slowest pair of each round sets everyone's pace (7B prefill
       // +30 %, FP8 72B +13 %, block-scaled 7B +73 % when paced)
-      const bool paced = leader && !kFp8 && !kDown && num_kb >= kPaceMinSlices;
+      const bool paced = leader && can_pace && !kFp8 && !kDown && num_kb >= kPaceMinSlices;
       bool pacing = paced;  // off for the rest of the launch once a wait runs out
       int round = 0;
       for (int t = pair; ok && t < num_tiles; t += pairs, ++round) {
@@ -593,6 +606,10 @@ cudaError_t configure_large_m_pair(int* max_pairs) {
 
 size_t large_m_pair_smem_bytes() { return PairCfg<false>::kSmem; }
 int large_m_pair_stages(bool mx) { return mx ? PairCfg<true>::kStages : PairCfg<false>::kStages; }
+
+cudaError_t large_m_pair_pace_run_out(unsigned long long* count) {
+  return cudaMemcpyFromSymbol(count, g_pace_run_out, sizeof(*count));
+}
 
 cudaError_t launch_large_m_pair(const LargeMParams& p, cudaStream_t stream) {
   if (p.grid < 2 || (p.grid % 2) != 0 || p.bn != PairCfg<false>::kBN) return cudaErrorInvalidValue;

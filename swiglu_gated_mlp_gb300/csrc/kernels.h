@@ -92,6 +92,9 @@ cudaError_t launch_large_m(const LargeMParams& p, cudaStream_t stream);
 cudaError_t configure_large_m_pair(int* max_pairs);
 size_t large_m_pair_smem_bytes();
 int large_m_pair_stages(bool mx = false);
+// Number of the pair kernel's tile-round pacing waits that ran out on the
+// current device since the library was loaded (a testing counter).
+cudaError_t large_m_pair_pace_run_out(unsigned long long* count);
 cudaError_t launch_large_m_pair(const LargeMParams& p, cudaStream_t stream);
 
 // K split over the two CTAs of a cluster, one 128 x 64 output tile per cluster

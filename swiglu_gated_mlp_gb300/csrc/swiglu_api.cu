@@ -1396,4 +1396,18 @@ void swiglu_testing_inject_stall(int enable, uint32_t timeout_ms) {
   if (timeout_ms) g_timeout_ns.store(uint64_t(timeout_ms) * 1000000ull);
 }
 
+swiglu_status_t swiglu_testing_pace_run_out(uint64_t* count) {
+  if (!count) return SWIGLU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  swiglu_status_t st = device_state(&d);
+  if (st != SWIGLU_OK) return st;
+  unsigned long long v = 0;
+  if (swg::large_m_pair_pace_run_out(&v) != cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_ERR_CUDA;
+  }
+  *count = static_cast<uint64_t>(v);
+  return SWIGLU_OK;
+}
+
 }  // extern "C"

@@ -352,9 +352,10 @@ def test_pair_kernel_launches_on_two_streams_at_once(native):
     # The pair kernel keeps its tile rounds loosely in step through per-round
     # counters in global memory, tagged per launch (bf16, K >= 8192). Two
     # launches in flight at once (separate streams) share those counters: each
-    # must still give the oracle's result (their pacing waits run out and
-    # stop; nothing else depends on them). 1024 x 8192 outputs: 256 tiles,
-    # about 3.4 rounds a pair, so the waits from round 2 on are exercised.
+    # must still give the oracle's result (a pacing wait that finds a later
+    # launch's counter, or runs out, only stops pacing). 1024 x 8192 outputs:
+    # 256 tiles, about 3.4 rounds a pair, so the waits from round 2 on are
+    # exercised.
     from oracle import compare
     from swiglu_gated_mlp_gb300.workloads import sample_rows
     M, K, N = 1024, 8192, 8192
@@ -375,3 +376,37 @@ def test_pair_kernel_launches_on_two_streams_at_once(native):
         ref = swiglu_f64(bf16_bits(a), bf16_bits(w1), bf16_bits(w2), rows=rows)
         rep = compare.report(bf16_bits(ys[i].cpu())[rows], ref)
         assert rep["nonfinite"] == 0 and rep["tolerance_pass"], rep
+
+
+def test_round_pacing_stays_aligned_after_a_small_grid(native):
+    # Launch numbers of the pair kernel's round pacing are drawn on the device
+    # from a global ticket, one fixed-size block per launch whatever its number
+    # of pairs. A launch with 16 pairs between paced launches (bf16, K = 8192,
+    # 512 tiles on 76 pairs: several rounds) must leave every paced launch
+    # with one launch number: none of their waits may run out (a misaligned
+    # number splits a launch in two, and then its waits run out every time).
+    from oracle import compare
+    from swiglu_gated_mlp_gb300.workloads import sample_rows
+    sm, sk, sn = 256, 1024, 2048
+    small = tuple(t.cuda() for t in make_inputs(sm, sk, sn, seed=41))
+    swp = native.swiglu_pack_weights(small[1], small[2])
+    ys = torch.empty(sm, sn, dtype=torch.bfloat16, device="cuda")
+    assert "grid=32 " in native.swiglu_plan_string(sm, sk, sn, PAIR) + " "
+    M, K, N = 2048, 8192, 8192
+    a, w1, w2 = make_inputs(M, K, N, seed=43)
+    ad = a.cuda()
+    wp = native.swiglu_pack_weights(w1.cuda(), w2.cuda())
+    assert native.swiglu_plan_string(M, K, N).startswith("large_m_pair")
+    y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+    before = native.swiglu_testing_pace_run_out()
+    for _ in range(3):
+        native.swiglu_forward_variant(small[0], swp, sn, PAIR, Y=ys)
+        native.swiglu_forward(ad, wp, N, Y=y)
+    torch.cuda.synchronize()
+    native.swiglu_check_device_status()
+    assert native.swiglu_testing_pace_run_out() == before
+    rows = sample_rows(M, 16, seed=7)
+    ref = swiglu_f64(bf16_bits(a), bf16_bits(w1), bf16_bits(w2), rows=rows)
+    rep = compare.report(bf16_bits(y.cpu())[rows], ref)
+    assert rep["nonfinite"] == 0 and rep["tolerance_pass"], rep
