@@ -362,7 +362,7 @@ SWIGLU_API swiglu_status_t swiglu_down_plan_string_ws(int64_t M, int64_t N, int6
  * other forward entry points allocate one small status record per device on
  * first use; this one runs the decode (small-M) kernel with that record in a
  * file-scope static device array of 256 bytes instead, held by every GPU that
- * loads the library until the process exits. The paper has no counterpart:
+ * loads the library until the process exits. No passage of the method covers it:
  * this is a deployment variant, not part of the method.
  *
  * Same arguments and result as swiglu_forward, for M <= 256 (larger M:

@@ -354,8 +354,8 @@ def test_pair_kernel_launches_on_two_streams_at_once(native):
     # launches in flight at once (separate streams) share those counters: each
     # must still give the oracle's result (a pacing wait that finds a later
     # launch's counter, or runs out, only stops pacing). 1024 x 8192 outputs:
-    # 256 tiles, about 3.4 rounds a pair, so the waits from round 2 on are
-    # exercised.
+    # 256 tiles, about 3.4 tile rounds a pair, so the waits before the third
+    # and fourth rounds are exercised.
     from oracle import compare
     from swiglu_gated_mlp_gb300.workloads import sample_rows
     M, K, N = 1024, 8192, 8192
