@@ -101,6 +101,25 @@ def _code_only(text: str) -> str:
     return "\n".join(line for line in lines if line)
 
 
+def host_copy_rates(a_host, a_dev, y_dev, y_host, stream, reps: int = 3) -> dict:
+    """This box's pinned host <-> device copy rates at the step's own sizes
+    (best of `reps` single copies, CUDA events on `stream`): the end-to-end
+    figure is bound by them when a step's copies outlast its kernel."""
+    def best(dst, src):
+        t = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                dst.copy_(src, non_blocking=True)
+                e1.record(stream)
+            e1.synchronize()
+            t.append(e0.elapsed_time(e1) * 1e-3)
+        return round(src.numel() * src.element_size() / min(t) / 1e9, 1)
+    return {"h2d_gbs": best(a_dev, a_host), "d2h_gbs": best(y_host, y_dev),
+            "how": "pinned host memory, one copy at a time, best of %d" % reps}
+
+
 def source_stamp() -> str:
     """Hash of the kernel sources' code (comments and blank lines left out)."""
     h = hashlib.sha256()
@@ -501,6 +520,7 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
         sa_host = [pr.host["sat"].pin_memory() for _ in a_host]
         sa_dev = [torch.empty_like(pr.host["sat"], device=dev) for _ in e2e_streams]
     e2e_steps = steps
+    copy_rates = host_copy_rates(a_host[0], a_dev[0], y_dev[0], y_host[0], stream)
 
     def e2e_step(i):
         j = i % len(a_host)
@@ -544,7 +564,7 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
            "h2d_bytes_per_step": a_cpu.numel() * a_cpu.element_size() + (
                pr.host["sat"].numel() if mx else 0),
            "d2h_bytes_per_step": 2 * M * out_cols,
-           "steps": e2e_steps, "streams": len(e2e_streams),
+           "steps": e2e_steps, "streams": len(e2e_streams), "copy_rates": copy_rates,
            "api": ("pinned-host copies + swiglu_down_forward" if down else
                    "pinned-host copies (A and its block scales) + swiglu_forward_mxfp8" if mx else
                    "pinned-host copies + swiglu_forward_fp8" if fp8 else

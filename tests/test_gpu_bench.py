@@ -32,6 +32,7 @@ def test_bench_line_has_the_contract_fields():
     assert abs(roof["avg_launch_us"] * 1e-3 - line["ms_per_step"]) < 1e-3
     e2e = line["e2e"]
     assert e2e["h2d_bytes_per_step"] == 2 * 128 * 896 and e2e["d2h_bytes_per_step"] == 2 * 128 * 4864
+    assert e2e["copy_rates"]["h2d_gbs"] > 0 and e2e["copy_rates"]["d2h_gbs"] > 0
     (sec,) = line["secondary"]
     assert sec["workload"] == "qwen2.5-7b-decode-m16" and sec["gpu_launches"] == 7
     assert sec["roofline"]["kernel"] == "fused_small_m_kernel" and sec["value"] > 0
