@@ -204,6 +204,33 @@ def test_largest_k_and_n_match_oracle(native, M, K, N):
     torch.cuda.empty_cache()
 
 
+# The largest M the ABI accepts (2^31 - 1 tokens, a ragged last row tile) on
+# the row-tiled kernels: row coordinates near 2^31 in the loads, stores and
+# tile loops. A is a seeded 4096-row block repeated down the rows, so each
+# sampled row's oracle is that of its row in the block (about 69 GB on the
+# device: A and Y, 34 GB each).
+@pytest.mark.parametrize("variant", [AUTO, LARGE, PAIR])
+def test_largest_m_matches_oracle(native, variant):
+    from oracle import compare
+    M, K, N, blk = (1 << 31) - 1, 8, 8, 4096
+    a, w1, w2 = make_inputs(blk, K, N, seed=61)
+    ad = y = None
+    try:
+        ad = a.cuda().repeat((M + blk - 1) // blk, 1)[:M]
+        wp = native.swiglu_pack_weights(w1.cuda(), w2.cuda())
+        y = native.swiglu_forward_variant(ad, wp, N, variant)
+        native.swiglu_check_device_status()
+        rows = np.array([0, 1, blk - 1, blk, 1 << 30, M - 257, M - 256, M - 129, M - 2, M - 1],
+                        dtype=np.int64)
+        got = bf16_bits(y[torch.from_numpy(rows).cuda()].cpu())
+        ref = swiglu_f64(bf16_bits(a), bf16_bits(w1), bf16_bits(w2), rows=rows % blk)
+        rep = compare.report(got, ref)
+        assert rep["nonfinite"] == 0 and rep["tolerance_pass"], rep
+    finally:
+        ad = y = None
+        torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("variant", [AUTO, LARGE, SMALL, PAIR, SEQ, SPLIT, RESIDENT])
 @pytest.mark.parametrize("M", [1, 9, 130])
 def test_smallest_k_and_n_match_oracle(native, variant, M):
