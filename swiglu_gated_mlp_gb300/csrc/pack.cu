@@ -146,7 +146,7 @@ cudaError_t launch_pack_mx_weight_scales(const void* s1, const void* s2, void* o
 
 cudaError_t launch_tile_mx_act_scales(const void* sa, void* out, int M, int K,
                                       cudaStream_t stream) {
-  const int m_blocks = (M + 127) / 128;
+  const int m_blocks = static_cast<int>((static_cast<int64_t>(M) + 127) / 128);  // M up to 2^31 - 1
   const int k_slices = (K + kBlockK8 - 1) / kBlockK8;
   tile_mx_act_scales_kernel<<<dim3(m_blocks, k_slices), 256, 0, stream>>>(
       static_cast<const uint8_t*>(sa), static_cast<uint8_t*>(out), M, (K + kMxGroup - 1) / kMxGroup,

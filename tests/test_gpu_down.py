@@ -66,6 +66,32 @@ def test_down_matches_oracle(native, M, N, H):
     run_down(native, M, N, H, seed=M + N + H)
 
 
+def test_down_largest_m_matches_oracle(native):
+    # 2^31 - 1 tokens (the largest M the ABI accepts) on the CTA-pair kernel,
+    # with the residual read at row offsets near 2^31: Y and R are seeded
+    # 4096-row blocks repeated down the rows, so each sampled row's oracle is
+    # its row in the block (about 103 GB on the device)
+    M, N, H, blk = (1 << 31) - 1, 8, 8, 4096
+    y, w3, r = down_inputs(blk, N, H, seed=73)
+    reps = (M + blk - 1) // blk
+    yd = rd = out = None
+    try:
+        yd = y.cuda().repeat(reps, 1)[:M]
+        rd = r.cuda().repeat(reps, 1)[:M]
+        wp = native.swiglu_pack_down_weights(w3.cuda())
+        out = native.swiglu_down_forward(yd, wp, H, R=rd)
+        native.swiglu_check_device_status()
+        rows = np.array([0, 1, blk - 1, blk, 1 << 30, M - 257, M - 256, M - 129, M - 2, M - 1],
+                        dtype=np.int64)
+        got = bf16_bits(out[torch.from_numpy(rows).cuda()].cpu())
+        ref = down_f64(bf16_bits(y), bf16_bits(w3), bf16_bits(r), rows=rows % blk)
+        rep = compare.report(got, ref)
+        assert rep["nonfinite"] == 0 and rep["tolerance_pass"], rep
+    finally:
+        yd = rd = out = None
+        torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("M", [16, 300])
 def test_down_without_residual(native, M):
     run_down(native, M, 1024, 520, seed=M + 1, residual=False)

@@ -68,6 +68,36 @@ def test_fp8_small_token_counts_match_oracle(native, M):
     run_fp8(native, M, 400, 264, seed=3000 + M)
 
 
+def _repeat_rows(t, M):
+    """The rows of a CPU block repeated down to M rows, on the device (bytes as uint8)."""
+    reps = (M + t.shape[0] - 1) // t.shape[0]
+    return t.cuda().view(torch.uint8).repeat(reps, 1)[:M].view(t.dtype)
+
+
+def test_fp8_largest_m_matches_oracle(native):
+    # 2^31 - 1 tokens (the largest M the ABI accepts) on the CTA-pair kernel:
+    # A is a seeded 4096-row block repeated down the rows, so each sampled
+    # row's oracle is its row in the block (about 69 GB on the device)
+    M, K, N, blk = (1 << 31) - 1, 16, 8, 4096
+    a8, w18, w28, (sa, s1, s2) = make_inputs_fp8(blk, K, N, seed=67)
+    ad = y = None
+    try:
+        ad = _repeat_rows(a8, M)
+        wp = native.swiglu_pack_weights_fp8(w18.cuda(), w28.cuda())
+        y = native.swiglu_forward_fp8(ad, wp, N, sa, s1, s2)
+        native.swiglu_check_device_status()
+        rows = np.array([0, 1, blk - 1, blk, 1 << 30, M - 257, M - 256, M - 129, M - 2, M - 1],
+                        dtype=np.int64)
+        got = bf16_bits(y[torch.from_numpy(rows).cuda()].cpu())
+        ref = swiglu_f64_fp8(fp8_bits(a8), fp8_bits(w18), fp8_bits(w28), sa, s1, s2,
+                             rows=rows % blk)
+        rep = compare.report(got, ref)
+        assert rep["nonfinite"] == 0 and rep["tolerance_pass"], rep
+    finally:
+        ad = y = None
+        torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("name", ["qwen2.5-7b-decode-m16", "qwen2.5-7b-prefill-m4096",
                                   "qwen2.5-72b-prefill-m8192"])
 def test_fp8_full_size_workloads(native, name):

@@ -114,6 +114,35 @@ def test_mx_small_token_counts_match_oracle(native, M):
     run_mx(native, M, 416, 264, seed=2000 + M)
 
 
+def test_mx_largest_m_matches_oracle(native):
+    # 2^31 - 1 tokens (the largest M the ABI accepts) on the CTA-pair kernel,
+    # with the activation-scale tiling at that size: A and its scales are a
+    # seeded 4096-row block repeated down the rows, so each sampled row's
+    # oracle is its row in the block (about 115 GB on the device)
+    M, K, N, blk = (1 << 31) - 1, 32, 8, 4096
+    a8, sa, w18, s1, w28, s2 = make_inputs_mxfp8(blk, K, N, seed=71)
+    reps = (M + blk - 1) // blk
+    ad = sad = sat = y = None
+    try:
+        ad = a8.cuda().view(torch.uint8).repeat(reps, 1)[:M].view(a8.dtype)
+        sad = sa.cuda().repeat(reps, 1)[:M]
+        wp = native.swiglu_pack_weights_mxfp8(w18.cuda(), s1.cuda(), w28.cuda(), s2.cuda())
+        sat = native.swiglu_pack_act_scales_mxfp8(sad)
+        sad = None
+        y = native.swiglu_forward_mxfp8(ad, sat, wp, N)
+        native.swiglu_check_device_status()
+        rows = np.array([0, 1, blk - 1, blk, 1 << 30, M - 257, M - 256, M - 129, M - 2, M - 1],
+                        dtype=np.int64)
+        got = bf16_bits(y[torch.from_numpy(rows).cuda()].cpu())
+        ref = swiglu_f64_mxfp8(fp8_bits(a8), sa.numpy(), fp8_bits(w18), s1.numpy(), fp8_bits(w28),
+                               s2.numpy(), rows=rows % blk)
+        rep = compare.report(got, ref)
+        assert rep["nonfinite"] == 0 and rep["tolerance_pass"], rep
+    finally:
+        ad = sad = sat = y = None
+        torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("M,K,N", [(16, 1024, 1280), (33, 416, 264), (64, 896, 4864),
                                    (16, 896, 4864), (300, 512, 1000), (512, 1024, 2048),
                                    (1000, 2048, 768)])
