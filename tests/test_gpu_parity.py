@@ -239,6 +239,37 @@ def test_smallest_k_and_n_match_oracle(native, variant, M):
 
 # ------------------------------------------------------- special values ----
 
+def test_empty_batch_on_every_entry_point(native):
+    # M = 0 tokens: every forward entry point (each bf16 variant, host buffers,
+    # per-tensor and block-scaled FP8, the down-projection with and without a
+    # workspace) returns an empty output and leaves the device status clean
+    from swiglu_gated_mlp_gb300.workloads import make_inputs_fp8, make_inputs_mxfp8
+    K, N, H = 256, 264, 264
+    _, w1, w2 = make_inputs(1, K, N, seed=5)
+    wp = native.swiglu_pack_weights(w1.cuda(), w2.cuda())
+    a0 = torch.empty(0, K, dtype=torch.bfloat16, device="cuda")
+    for variant in (AUTO, LARGE, SMALL, PAIR, SEQ, SPLIT, RESIDENT):
+        assert tuple(native.swiglu_forward_variant(a0, wp, N, variant).shape) == (0, N)
+    y_host = torch.empty(0, N, dtype=torch.bfloat16)
+    native.swiglu_forward_from_host(torch.empty(0, K, dtype=torch.bfloat16), wp, N, y_host, a0,
+                                    torch.empty(0, N, dtype=torch.bfloat16, device="cuda"))
+    a8, w18, w28, scales = make_inputs_fp8(1, K, N, seed=6)
+    wp8 = native.swiglu_pack_weights_fp8(w18.cuda(), w28.cuda())
+    assert tuple(native.swiglu_forward_fp8(a8.cuda()[:0], wp8, N, *scales).shape) == (0, N)
+    a8, sa, w18, s1, w28, s2 = make_inputs_mxfp8(1, K, N, seed=7)
+    wpm = native.swiglu_pack_weights_mxfp8(w18.cuda(), s1.cuda(), w28.cuda(), s2.cuda())
+    sat = native.swiglu_pack_act_scales_mxfp8(sa.cuda()[:0])
+    assert tuple(native.swiglu_forward_mxfp8(a8.cuda()[:0], sat, wpm, N).shape) == (0, N)
+    _, w3, _ = make_inputs(1, N, H, seed=8)
+    w3p = native.swiglu_pack_down_weights(w3.cuda())
+    y0 = torch.empty(0, N, dtype=torch.bfloat16, device="cuda")
+    assert tuple(native.swiglu_down_forward(y0, w3p, H).shape) == (0, H)
+    ws = native.swiglu_down_workspace(16, N, H)
+    assert tuple(native.swiglu_down_forward(y0, w3p, H, workspace=ws).shape) == (0, H)
+    torch.cuda.synchronize()
+    native.swiglu_check_device_status()
+
+
 @pytest.mark.parametrize("variant", [LARGE, SMALL])
 def test_zero_activations_give_exact_zero(native, variant):
     _, w1, w2 = make_inputs(1, 256, 384, seed=4)
