@@ -406,30 +406,33 @@ def test_plan_string_names_a_kernel(native):
     assert native.swiglu_plan_string(4096, 3584, 18944, 1).startswith("large_m bn=128")
 
 
-def test_pair_kernel_launches_on_two_streams_at_once(native):
+@pytest.mark.parametrize("n_streams", [2, 3])
+def test_pair_kernel_launches_on_several_streams_at_once(native, n_streams):
     # The pair kernel keeps its tile rounds loosely in step through per-round
-    # counters in global memory, tagged per launch (bf16, K >= 8192). Two
-    # launches in flight at once (separate streams) share those counters: each
-    # must still give the oracle's result (a pacing wait that finds a later
-    # launch's counter, or runs out, only stops pacing). 1024 x 8192 outputs:
-    # 256 tiles, about 3.4 tile rounds a pair, so the waits before the third
-    # and fourth rounds are exercised.
+    # counters in global memory, tagged per launch (bf16, K >= 8192). Launches
+    # in flight at once (separate streams) share those counters; with three
+    # streams the CTAs of two launches can also start interleaved and draw
+    # from each other's launch numbers. Each launch must still give the
+    # oracle's result (a pacing wait that finds a later launch's counter, or
+    # runs out, only stops pacing). 1024 x 8192 outputs: 256 tiles, about 3.4
+    # tile rounds a pair, so the waits before the third and fourth rounds are
+    # exercised.
     from oracle import compare
     from swiglu_gated_mlp_gb300.workloads import sample_rows
     M, K, N = 1024, 8192, 8192
-    inputs = [make_inputs(M, K, N, seed=31 + i) for i in range(2)]
+    inputs = [make_inputs(M, K, N, seed=31 + i) for i in range(n_streams)]
     dev = [tuple(t.cuda() for t in x) for x in inputs]
     wps = [native.swiglu_pack_weights(w1, w2) for _, w1, w2 in dev]
-    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
-    ys = [torch.empty(M, N, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    streams = [torch.cuda.Stream() for _ in range(n_streams)]
+    ys = [torch.empty(M, N, dtype=torch.bfloat16, device="cuda") for _ in range(n_streams)]
     torch.cuda.synchronize()
     for _ in range(4):
-        for i in range(2):
+        for i in range(n_streams):
             native.swiglu_forward_variant(dev[i][0], wps[i], N, PAIR, Y=ys[i], stream=streams[i])
     torch.cuda.synchronize()
     native.swiglu_check_device_status()
     rows = sample_rows(M, 64, seed=5)
-    for i in range(2):
+    for i in range(n_streams):
         a, w1, w2 = inputs[i]
         ref = swiglu_f64(bf16_bits(a), bf16_bits(w1), bf16_bits(w2), rows=rows)
         rep = compare.report(bf16_bits(ys[i].cpu())[rows], ref)
