@@ -38,10 +38,12 @@
 // per launch at the same time (lag 1: much slower; lag 4: more reads).
 // Shorter tiles lose time when paced, since the slowest pair of each round
 // then sets everyone's pace. Consecutive rounds share their A rows (a row
-// group's tiles run down the columns), so odd rounds walk K backwards and
-// start on the A slices the previous round loaded last, while L2 still holds
-// them: the paced 72B prefill read 8.0 -> 6.3 GB and ran 2 % faster; unpaced
-// shapes, whose pairs drift apart by whole rounds, were unchanged.
+// group's tiles run down the columns), so on the paced shapes odd rounds
+// walk K backwards and start on the A slices the previous round loaded last,
+// while L2 still holds them: the 72B prefill read 8.0 -> 6.3 GB and ran 2 %
+// faster. Unpaced launches keep one direction: their pairs drift apart by
+// whole rounds, so the tiles in flight would mix both directions (before the
+// pacing, alternating directions raised the reads of both 72B forms).
 //
 // With kDown the same pipeline computes the MLP's down-projection
 // Out = Y x W3 + R: a tile is 256 consecutive output columns (rank r loads
@@ -242,7 +244,8 @@ __global__ void __launch_bounds__(PairCfg<kMx>::kThreadsT, 1)
       // only long bf16 gate/up tiles (K >= 8192, the 72B shape): with shorter
       // tiles the slowest pair of each round sets everyone's pace (7B prefill
       // +30 %, FP8 72B +13 %, block-scaled 7B +73 % when paced)
-      const bool paced = leader && can_pace && !kFp8 && !kDown && num_kb >= kPaceMinSlices;
+      const bool long_tiles = !kFp8 && !kDown && num_kb >= kPaceMinSlices;  // same in both CTAs
+      const bool paced = leader && can_pace && long_tiles;
       bool pacing = paced;  // off for the rest of the launch once a wait runs out
       int round = 0;
       for (int t = pair; ok && t < num_tiles; t += pairs, ++round) {
@@ -255,9 +258,9 @@ __global__ void __launch_bounds__(PairCfg<kMx>::kThreadsT, 1)
         const int m0 = mb * 2 * kTileM + static_cast<int>(rank) * kTileM;
         const int wtile = nb * num_kb;                        // (column block nb, K slice 0)
         const int wrow = static_cast<int>(rank) * kPackBlockN;  // gate rows (0) / up rows (1)
-        // odd rounds walk K backwards: they start on the A slices the previous
-        // round (same row tiles) read last, while those are still in L2
-        const bool backwards = (round & 1) != 0;
+        // paced shapes: odd rounds walk K backwards and start on the A slices
+        // the previous round (same row tiles) read last, while L2 holds them
+        const bool backwards = long_tiles && (round & 1) != 0;
         for (int i = 0; i < num_kb; ++i) {
           const int kb = backwards ? num_kb - 1 - i : i;
           if (!mbar_wait(empty0 + 8u * s, ph ^ 1u, wc, kSiteProducerEmpty)) {
