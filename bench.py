@@ -559,17 +559,59 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int):
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
     barrier(world)
+
+    def compute(i, b, st):  # the step's kernel on device buffers, as in e2e_step
+        if down:
+            sg.swiglu_down_forward(a_dev[b], wps[i % copies], K, R=Rs[i % copies], Out=y_dev[b],
+                                   stream=st, workspace=e2e_ws[b])
+        elif mx:
+            sg.swiglu_forward_mxfp8(a_dev[b], sa_dev[b], wps[i % copies], N, Y=y_dev[b], stream=st)
+        elif fp8:
+            sg.swiglu_forward_fp8(a_dev[b], wps[i % copies], N, *pr.host["scales"], Y=y_dev[b],
+                                  stream=st)
+        else:
+            sg.swiglu_forward(a_dev[b], wps[i % copies], N, Y=y_dev[b], stream=st)
+
+    # Where an end-to-end step's time goes: a few more steps on the same two
+    # streams and buffers, after the timed region, with events between the
+    # host-to-device copy, the kernel and the device-to-host copy. A phase's
+    # time includes any wait behind the other stream's work (copy engines, SMs).
+    phase_ev = []
+    for i in range(4):
+        b, j = i % len(e2e_streams), i % len(a_host)
+        st = e2e_streams[b]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        with torch.cuda.stream(st):
+            ev[0].record(st)
+            a_dev[b].copy_(a_host[j], non_blocking=True)
+            if mx:
+                sa_dev[b].copy_(sa_host[j], non_blocking=True)
+            ev[1].record(st)
+            compute(i, b, st)
+            ev[2].record(st)
+            y_host[j].copy_(y_dev[b], non_blocking=True)
+            ev[3].record(st)
+        phase_ev.append(ev)
+    torch.cuda.synchronize()
+
+    def phase_ms(k):
+        return round(sum(e[k].elapsed_time(e[k + 1]) for e in phase_ev) / len(phase_ev), 3)
+    phases = {"h2d_ms": phase_ms(0), "kernel_ms": phase_ms(1), "d2h_ms": phase_ms(2),
+              "steps": len(phase_ev),
+              "how": "4 steps after the timed region on the same two streams, CUDA events "
+                     "between the phases; each includes waits behind the other stream"}
     sg.swiglu_check_device_status(stream=stream)
     e2e = {"value": round(aggregate(pr.flops, e2e_steps, e2e_s, world), 3), "unit": "TFLOP/s",
            "h2d_bytes_per_step": a_cpu.numel() * a_cpu.element_size() + (
                pr.host["sat"].numel() if mx else 0),
            "d2h_bytes_per_step": 2 * M * out_cols,
            "steps": e2e_steps, "streams": len(e2e_streams), "copy_rates": copy_rates,
+           "phases": phases,
            "api": ("pinned-host copies + swiglu_down_forward" if down else
                    "pinned-host copies (A and its block scales) + swiglu_forward_mxfp8" if mx else
                    "pinned-host copies + swiglu_forward_fp8" if fp8 else
                    "swiglu_forward_from_host")}
-    del a_dev, y_dev, a_host, y_host, wps, Rs, e2e_step
+    del a_dev, y_dev, a_host, y_host, wps, Rs, e2e_step, compute, phase_ev
 
     tensor_peak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
     out = {

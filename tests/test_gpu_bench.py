@@ -33,6 +33,7 @@ def test_bench_line_has_the_contract_fields():
     e2e = line["e2e"]
     assert e2e["h2d_bytes_per_step"] == 2 * 128 * 896 and e2e["d2h_bytes_per_step"] == 2 * 128 * 4864
     assert e2e["copy_rates"]["h2d_gbs"] > 0 and e2e["copy_rates"]["d2h_gbs"] > 0
+    assert all(e2e["phases"][k] > 0 for k in ("h2d_ms", "kernel_ms", "d2h_ms"))
     (sec,) = line["secondary"]
     assert sec["workload"] == "qwen2.5-7b-decode-m16" and sec["gpu_launches"] == 7
     assert sec["roofline"]["kernel"] == "fused_small_m_kernel" and sec["value"] > 0
